@@ -1,0 +1,425 @@
+#!/usr/bin/env python3
+"""Benchmark: throughput of the half-precision GEMM hot path on GB300.
+
+One step = one C = A . B through the C ABI (hgemm_run) on the workload's full
+shape.  Default workload: M = N = K = 4096, bf16 inputs, fp32 accumulate, bf16
+output, TN layout; metric TFLOPS = 2MNK / t.  The skinny workload reports GB/s
+of compulsory traffic instead.
+
+Timing: W untimed warm-up steps, then exactly K steps bracketed by a barrier
+and torch.cuda.synchronize on both sides, timed with CUDA events on the
+launching stream.  Inputs rotate through enough copies that the bytes touched
+between two uses of the same copy exceed twice the L2, so every step reads its
+operands from HBM.  SM clocks and throttle reasons are sampled with
+nvidia-smi during the timed region.  The end-to-end figure (e2e) is the same
+metric with the host->device copy of A and B from pinned memory and the
+device->host copy of C inside the timed region.
+
+N > 1 (torchrun): independent replicas, one per GPU, each running the full
+workload (weak scaling); the time is the maximum over ranks.
+
+--impl reference: the CPU oracle timed on the host cores on a bounded sample
+(a block of rows of C) of the same workload; that is the reference arm.
+
+Prints one JSON line (rank 0).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC_TFLOPS = "TFLOPS (2MNK/t) at M=N=K=4096 bf16, fp32 acc; % of dense BF16 tensor peak"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+THROTTLE_BITS = {  # nvidia-smi clocks_event_reasons bit masks
+    0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
+    0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+    0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
+KERNEL_SOURCES = ["tensor_core_half_gb300/csrc/gemm_dense.cu", "tensor_core_half_gb300/csrc/gemm_splitk.cu",
+                  "tensor_core_half_gb300/csrc/ptx.cuh", "tensor_core_half_gb300/csrc/desc.cuh",
+                  "tensor_core_half_gb300/csrc/sched.cuh", "tensor_core_half_gb300/csrc/kernels.h"]
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def load_traffic(workload: str, variant: int):
+    """DRAM bytes per launch from a committed ncu summary, if it matches these kernels."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get("%s/%d" % (workload, variant))
+    if not e or e.get("kernel_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------- clocks ----
+class ClockSampler:
+    """nvidia-smi sampling in the background; marks let us keep only samples
+    taken inside the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 50):
+        self.samples = []  # (host time, sm_mhz, max_mhz, power_w, active_mask)
+        self.proc = None
+        self.thread = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", str(period_ms)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._reader, daemon=True)
+        self.thread.start()
+
+    def _reader(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 5:
+                continue
+            try:
+                sm = float(parts[1])
+                mx = float(parts[2])
+                pw = float(parts[3]) if parts[3] not in ("[N/A]", "N/A") else float("nan")
+                act = int(parts[4], 16) if parts[4].startswith("0x") else int(parts[4])
+            except ValueError:
+                continue
+            self.samples.append((time.time(), sm, mx, pw, act))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        window = "timed"
+        if not inside:  # timed region shorter than the sampling period: nearest samples
+            inside = sorted(self.samples, key=lambda s: min(abs(s[0] - t0), abs(s[0] - t1)))[:3]
+            window = "nearest"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "window": "none"}
+        sms = sorted(s[1] for s in inside)
+        mask = 0
+        for s in inside:
+            mask |= s[4]
+        reasons = [name for bit, name in THROTTLE_BITS.items() if mask & bit]
+        pw = [s[3] for s in inside if not math.isnan(s[3])]
+        return {"sm_mhz": sms[len(sms) // 2], "sm_max_mhz": max(s[2] for s in inside), "reasons": reasons,
+                "power_w_max": max(pw) if pw else None, "samples": len(inside), "window": window}
+
+
+# --------------------------------------------------------------- helpers ----
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def workload_metric(w):
+    """(metric name, unit, per-step amount of the unit's numerator, roofline bound)."""
+    if w.name.startswith("skinny"):
+        return ("GB/s of compulsory traffic (A + B + C bytes / t) at M=%d N=%d K=%d %s" % (w.M, w.N, w.K, w.in_dtype),
+                "GB/s", float(w.compulsory_bytes) / 1e9, "hbm")
+    if w.name == "square4096_bf16":
+        return METRIC_TFLOPS, "TFLOPS", float(w.flops) / 1e12, "tensor"
+    return ("TFLOPS (2MNK/t) at M=%d N=%d K=%d %s, %s acc" % (w.M, w.N, w.K, w.in_dtype, w.acc_dtype), "TFLOPS",
+            float(w.flops) / 1e12, "tensor")
+
+
+def cpu_oracle_sample(w, a_bits, b_bits, target_s: float):
+    """Times the oracle (as it stands, all host cores) on a block of rows of C."""
+    import numpy as np
+
+    import oracle
+    cores = os.cpu_count() or 1
+    rows = 8
+    while True:
+        t0 = time.perf_counter()
+        oracle.gemm_entries(a_bits, b_bits, w.M, w.N, w.K, w.layout, w.in_dtype,
+                            np.repeat(np.arange(rows, dtype=np.int64), w.N),
+                            np.tile(np.arange(w.N, dtype=np.int64), rows), nthreads=cores)
+        dt = time.perf_counter() - t0
+        if dt >= target_s or rows >= w.M:
+            return rows, dt, cores
+        rows = min(w.M, max(rows * 2, int(rows * target_s / max(dt, 1e-3) * 1.1)))
+
+
+# ------------------------------------------------------------------ main ----
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=None)
+    ap.add_argument("--variant", default="auto")
+    ap.add_argument("--e2e-steps", type=int, default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world, rank, local = dist_setup()
+    from tensor_core_half_gb300 import workloads
+    w = workloads.WORKLOADS[args.workload or workloads.HEADLINE]
+    metric, unit, per_step, bound = workload_metric(w)
+
+    if args.impl == "reference":
+        run_reference(args, w, metric, unit, per_step, world, rank)
+        return
+
+    import numpy as np
+    import torch
+
+    from tensor_core_half_gb300 import hgemm
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    a_cpu, b_cpu = workloads.generate_workload(w)
+    dt = workloads.DTYPES[w.out_dtype]
+    in_bytes = (a_cpu.numel() + b_cpu.numel()) * 2
+    c_bytes = w.M * w.N * 2
+    copies = max(1, math.ceil(2 * L2_BYTES / max(1, in_bytes + c_bytes)))
+    A = [a_cpu.to(dev) for _ in range(copies)]
+    B = [b_cpu.to(dev) for _ in range(copies)]
+    C = [torch.empty((w.M, w.N), dtype=dt, device=dev) for _ in range(copies)]
+    handle = hgemm.Handle()
+    handle.set_option(hgemm.HGEMM_OPT_FORCE_VARIANT, hgemm.VARIANTS[args.variant])
+    st, plan = hgemm.hgemm_plan(w.M, w.N, w.K, hgemm.LAYOUTS[w.layout], hgemm.DTYPES[w.in_dtype],
+                                hgemm.DTYPES[w.acc_dtype], hgemm.DTYPES[w.out_dtype],
+                                torch.cuda.get_device_properties(dev).multi_processor_count,
+                                hgemm.VARIANTS[args.variant])
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+    lay, fin, facc, fout = (hgemm.LAYOUTS[w.layout], hgemm.DTYPES[w.in_dtype], hgemm.DTYPES[w.acc_dtype],
+                            hgemm.DTYPES[w.out_dtype])
+    ptrs = [(A[i].data_ptr(), B[i].data_ptr(), C[i].data_ptr()) for i in range(copies)]
+
+    def step(i):
+        a, b, c = ptrs[i % copies]
+        s = hgemm.hgemm_run(handle.h, a, b, c, w.M, w.N, w.K, lay, fin, facc, fout, sp)
+        if s != hgemm.HGEMM_OK:
+            raise hgemm.HgemmError(s, "hgemm_run")
+
+    for i in range(args.warmup):
+        step(i)
+    st, detail = handle.sync_status()
+    if st != hgemm.HGEMM_OK:
+        raise hgemm.HgemmError(st, "warm-up (detail %s)" % hex(detail))
+
+    # ------------------------------------------------ device-timed region ----
+    sampler = ClockSampler(local)
+    time.sleep(0.3)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    h0 = time.time()
+    t_start.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        step(i)
+        ev[i][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    h1 = time.time()
+    barrier(world)
+    st, detail = handle.sync_status()
+    if st != hgemm.HGEMM_OK:
+        raise hgemm.HgemmError(st, "timed region (detail %s)" % hex(detail))
+    total_ms = t_start.elapsed_time(t_end)
+    per_launch = sorted(e[0].elapsed_time(e[1]) for e in ev)
+    kernel_ms_avg = sum(per_launch) / len(per_launch)
+    median_ms = per_launch[len(per_launch) // 2]
+    total_ms_max = max_over_ranks(total_ms, world)
+    time.sleep(0.2)
+    sampler.stop()
+    clocks = sampler.summary(h0, h1)
+
+    # ------------------------------------------------------ end to end ------
+    e2e_steps = args.e2e_steps if args.e2e_steps is not None else max(3, min(args.steps, 50))
+    a_pin = a_cpu.pin_memory()
+    b_pin = b_cpu.pin_memory()
+    c_pin = torch.empty((w.M, w.N), dtype=dt).pin_memory()
+    Ad, Bd, Cd = A[0], B[0], C[0]
+
+    def e2e_step():
+        Ad.copy_(a_pin, non_blocking=True)
+        Bd.copy_(b_pin, non_blocking=True)
+        s = hgemm.hgemm_run(handle.h, Ad.data_ptr(), Bd.data_ptr(), Cd.data_ptr(), w.M, w.N, w.K, lay, fin, facc,
+                            fout, sp)
+        if s != hgemm.HGEMM_OK:
+            raise hgemm.HgemmError(s, "hgemm_run (e2e)")
+        c_pin.copy_(Cd, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    st, detail = handle.sync_status()
+    if st != hgemm.HGEMM_OK:
+        raise hgemm.HgemmError(st, "e2e (detail %s)" % hex(detail))
+
+    if rank != 0:
+        handle.close()
+        return
+
+    value = world * args.steps * per_step / (total_ms_max / 1e3)
+    e2e_value = world * e2e_steps * per_step / (e2e_ms / 1e3)
+    peaks, peak_src = load_peaks()
+    timed_seconds = total_ms / 1e3
+    if bound == "tensor":
+        sustained = timed_seconds > 1.0
+        peak = peaks.get("bf16_tflops_sustained" if sustained else "bf16_tflops")
+        achieved = (w.flops / 1e12) / (kernel_ms_avg / 1e3)
+        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4), "peak_source": "%s %s" % (peak_src,
+                                                                             "sustained" if sustained else "burst")}
+    else:
+        peak = peaks.get("hbm_gbs")
+        achieved = (w.compulsory_bytes / 1e9) / (kernel_ms_avg / 1e3)
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "peak_source": peak_src}
+    roof["traffic"] = load_traffic(w.name, plan.variant)
+    roof["kernel_ms_avg"] = round(kernel_ms_avg, 5)
+
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        rows, secs, cores = cpu_oracle_sample(w, workloads.bits(a_cpu), workloads.bits(b_cpu), args.cpu_seconds)
+        frac = rows / w.M
+        cpu_val = (per_step * frac) / secs
+        cpu = {"value": round(cpu_val, 6), "unit": unit, "cores": cores, "kind": "oracle",
+               "sample": "first %d of %d rows of C (%.3g s, fp64 oracle, %d threads)" % (rows, w.M, secs, cores)}
+
+    out = {
+        "metric": metric, "value": round(value, 3), "unit": unit, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(total_ms_max / args.steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.in_dtype, "data": "synthetic",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "layout": w.layout, "in": w.in_dtype,
+                   "acc": w.acc_dtype, "out": w.out_dtype, "variant": list(hgemm.VARIANTS)[plan.variant],
+                   "grid": plan.grid, "tile": [plan.tile_m, plan.tile_n], "stages": plan.stages,
+                   "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "inputs rotate over %d copies (%.0f MiB > 2x L2)" % (copies, copies * (in_bytes + c_bytes) / 2**20),
+                   "median_step_ms": round(median_ms, 5),
+                   "value_at_median": round(per_step / (median_ms / 1e3), 3)},
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(e2e_value, 3), "unit": unit, "h2d_bytes_per_step": int(in_bytes),
+                "d2h_bytes_per_step": int(c_bytes), "steps": e2e_steps},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    handle.close()
+    print(json.dumps(out), flush=True)
+
+
+def run_reference(args, w, metric, unit, per_step, world, rank):
+    """The CPU oracle on the same workload: each step computes a bounded block of rows."""
+    if world > 1 and rank != 0:
+        return
+    import numpy as np
+
+    import oracle
+    from tensor_core_half_gb300 import workloads
+    a, b = workloads.generate_workload(w)
+    ab, bb = workloads.bits(a), workloads.bits(b)
+    cores = os.cpu_count() or 1
+    # rows per step: sized so that warm-up plus K steps take about 90 s of oracle work
+    per_step_s = max(0.02, min(0.5, 90.0 / (args.steps + min(args.warmup, 3))))
+    rows, secs, _ = cpu_oracle_sample(w, ab, bb, per_step_s)
+    ri = np.repeat(np.arange(rows, dtype=np.int64), w.N)
+    ci = np.tile(np.arange(w.N, dtype=np.int64), rows)
+    for _ in range(min(args.warmup, 3)):
+        oracle.gemm_entries(ab, bb, w.M, w.N, w.K, w.layout, w.in_dtype, ri, ci, nthreads=cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.gemm_entries(ab, bb, w.M, w.N, w.K, w.layout, w.in_dtype, ri, ci, nthreads=cores)
+    total = time.perf_counter() - t0
+    frac = rows / w.M
+    value = args.steps * per_step * frac / total
+    sample = "first %d of %d rows of C per step (fp64 oracle, %d threads)" % (rows, w.M, cores)
+    out = {"impl": "reference", "metric": metric, "value": round(value, 6), "unit": unit, "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * total / args.steps, 3),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "layout": w.layout, "in": w.in_dtype},
+           "cpu_baseline": {"value": round(value, 6), "unit": unit, "cores": cores, "kind": "oracle",
+                            "sample": sample},
+           "e2e": {"value": round(value, 6), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+           "gpu_launches": 0}
+    print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,200 @@
+/*
+ * hgemm.h -- C ABI of a GB300 (sm_103a) dense half-precision matrix multiply
+ *
+ *     C[M,N] = A[M,K] . B[K,N]
+ *
+ * with fp16 or bf16 inputs, fp32 (or, for fp16 inputs, fp16) accumulation and
+ * fp16 or bf16 output, computed by hand-written tcgen05 / TMA kernels.
+ *
+ * The operation is the plain matrix product of "tcgen05 for dummies: a B200
+ * GEMM from scratch" (translated), section "Recap: how to write a fast matmul
+ * kernel": every C[m][n] is the dot product of row m of A and column n of B.
+ * Layout names follow "HGEMM: WMMA and MMA PTX study notes" (kernel header
+ * comment): TN = A row-major, B column-major (stored as [N,K]), C row-major;
+ * NN = A, B and C all row-major.
+ *
+ * Conventions shared by every entry point:
+ *   - All pointers passed to hgemm_run are DEVICE pointers of the device that
+ *     was current when the handle was created.  The caller owns them.
+ *   - Matrices are dense and packed (no leading-dimension arguments).
+ *   - A stream argument is a cudaStream_t passed as void* (0 = legacy default
+ *     stream).  Work is enqueued on it; nothing blocks the host except
+ *     hgemm_sync_status.
+ *   - Every entry point returns an hgemm_status_t; argument errors are
+ *     detected on the host before anything is launched and leave the device
+ *     untouched.  There is no CPU fallback and no vendor GEMM library call.
+ *   - A handle is not thread-safe: use one handle per host thread.
+ */
+#ifndef HGEMM_H_
+#define HGEMM_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct hgemm_ctx* hgemm_handle_t;
+
+typedef enum {
+  HGEMM_OK = 0,
+  HGEMM_ERR_INVALID_ARG = 1, /* null handle/pointer, negative size, bad enum, size too large */
+  HGEMM_ERR_UNSUPPORTED = 2, /* valid combination this library does not implement, or not sm_103 */
+  HGEMM_ERR_MISALIGNED = 3,  /* a base pointer is not 16-byte aligned, or a row pitch is not a
+                                multiple of 16 bytes (K % 8 != 0 or N % 8 != 0) */
+  HGEMM_ERR_ALIAS = 4,       /* C overlaps A or B */
+  HGEMM_ERR_NO_DEVICE = 5,   /* no CUDA device / driver */
+  HGEMM_ERR_CUDA = 6,        /* a CUDA runtime or driver call failed */
+  HGEMM_ERR_TIMEOUT = 7,     /* a bounded device-side wait gave up (reported by hgemm_sync_status) */
+  HGEMM_ERR_OOM = 8          /* workspace allocation failed */
+} hgemm_status_t;
+
+typedef enum { HGEMM_LAYOUT_TN = 0, HGEMM_LAYOUT_NN = 1 } hgemm_layout_t;
+
+typedef enum { HGEMM_F16 = 0, HGEMM_BF16 = 1, HGEMM_F32 = 2 } hgemm_dtype_t;
+
+/* Kernel variants (hgemm_plan / HGEMM_OPT_FORCE_VARIANT). */
+typedef enum {
+  HGEMM_VARIANT_AUTO = 0,
+  HGEMM_VARIANT_1SM_128x128 = 1, /* persistent tcgen05, one CTA per 128x128 C tile          */
+  HGEMM_VARIANT_1SM_128x256 = 2, /* persistent tcgen05, one CTA per 128x256 C tile          */
+  HGEMM_VARIANT_2SM_256x256 = 3, /* persistent tcgen05 cta_group::2, a CTA pair per 256x256 */
+  HGEMM_VARIANT_SPLITK = 4       /* skinny M (TN, fp32 accumulate, M <= 64): swap-AB split-K */
+} hgemm_variant_t;
+
+/* Handle options (hgemm_set_option). */
+typedef enum {
+  HGEMM_OPT_FORCE_VARIANT = 1, /* value: an hgemm_variant_t; AUTO restores automatic choice   */
+  HGEMM_OPT_TIMEOUT_NS = 2,    /* value: limit of every device-side wait, ns (default 2e9)    */
+  HGEMM_OPT_INJECT_FAULT = 3,  /* value: 0 off; 1 = the first CTA's producer drops its first
+                                  stage, so the consumer's bounded wait must give up (tests)  */
+  HGEMM_OPT_GROUP_M = 4,       /* value: rasterisation group height in tiles (default 8)      */
+  HGEMM_OPT_MAX_CTAS = 5       /* value: cap on persistent CTAs (0 = one per SM)              */
+} hgemm_option_t;
+
+/*
+ * hgemm_create -- bind a new handle to the CURRENT CUDA device.
+ *   out: receives the handle (owned by the caller, release with hgemm_destroy).
+ * The device must be compute capability 10.3 (sm_103).  Allocates a 16-byte
+ * device status word.  Returns NO_DEVICE when no device/driver is usable,
+ * UNSUPPORTED for another architecture, CUDA on any other CUDA failure.
+ */
+hgemm_status_t hgemm_create(hgemm_handle_t* out);
+
+/*
+ * hgemm_destroy -- synchronise the handle's device and free everything the
+ * handle owns (status word, split-K workspace).  Null is accepted (no-op).
+ */
+hgemm_status_t hgemm_destroy(hgemm_handle_t h);
+
+/*
+ * hgemm_run -- enqueue C = A . B on `stream`.
+ *   A: device pointer, M x K, row-major (element [m][k] at A + m*K + k).
+ *   B: device pointer; TN: stored N x K row-major (element B[k][n] at B + n*K + k);
+ *      NN: stored K x N row-major (element B[k][n] at B + k*N + n).
+ *   C: device pointer, M x N, row-major, written (never read).  Must not overlap A or B.
+ *   M, N, K >= 0, each <= 2^31 - 1.  M == 0 or N == 0: nothing to do, HGEMM_OK.
+ *      K == 0: C is filled with +0 (the empty sum).
+ *   in_dtype:  HGEMM_F16 or HGEMM_BF16 (A and B share it).
+ *   acc_dtype: HGEMM_F32, or HGEMM_F16 with in_dtype == HGEMM_F16.
+ *   out_dtype: HGEMM_F16 or HGEMM_BF16; the result is rounded to nearest even.
+ * Alignment: A, B, C 16-byte aligned; K % 8 == 0 and N % 8 == 0 (every row
+ * pitch is a multiple of 16 bytes, a TMA requirement).  K == 0 skips the K
+ * check and A, B may then be null.
+ * Asynchronous: returns once the kernel is enqueued.  A device-side timeout
+ * is reported later by hgemm_sync_status.  Split-K launches use a workspace
+ * that the handle allocates on first use (cudaMalloc; HGEMM_ERR_OOM on
+ * failure); consecutive launches on different streams must not overlap when
+ * they share a handle.
+ */
+hgemm_status_t hgemm_run(hgemm_handle_t h, const void* A, const void* B, void* C, int64_t M, int64_t N,
+                         int64_t K, hgemm_layout_t layout, hgemm_dtype_t in_dtype, hgemm_dtype_t acc_dtype,
+                         hgemm_dtype_t out_dtype, void* stream);
+
+/*
+ * hgemm_sync_status -- synchronise `stream`, then return and clear the device
+ * status word: HGEMM_OK, or HGEMM_ERR_TIMEOUT when a bounded wait in any
+ * kernel launched through this handle gave up since the last call (the
+ * launch's output is then undefined), or HGEMM_ERR_CUDA when the stream
+ * reports an error.  *detail (nullable) receives the raw status word: bits
+ * 0-7 the status, bits 8-15 the role that gave up (1 producer, 2 MMA issuer,
+ * 3 epilogue, 4 teardown), bits 16-31 the CTA index.
+ */
+hgemm_status_t hgemm_sync_status(hgemm_handle_t h, void* stream, int32_t* detail);
+
+/* Set a handle option (hgemm_option_t).  INVALID_ARG for an unknown option or value. */
+hgemm_status_t hgemm_set_option(hgemm_handle_t h, int32_t option, int64_t value);
+
+/* Static, human-readable name of a status code. */
+const char* hgemm_status_string(hgemm_status_t s);
+
+/* ------------------------------------------------------------------------- */
+/* Planning and introspection (host only; no device needed).                  */
+
+typedef struct {
+  int32_t variant;       /* hgemm_variant_t chosen                                        */
+  int32_t cta_group;     /* 1, or 2 for the CTA-pair MMA                                 */
+  int32_t tile_m;        /* C rows per tile (per CTA pair for cta_group 2); split-K: N rows */
+  int32_t tile_n;        /* C columns per tile; split-K: padded M (the MMA N)            */
+  int32_t block_k;       /* K elements per pipeline stage                                */
+  int32_t stages;        /* shared-memory ring depth                                     */
+  int32_t tiles_m;       /* tile grid                                                    */
+  int32_t tiles_n;
+  int32_t num_tiles;
+  int32_t k_blocks;      /* ceil(K / block_k)                                            */
+  int32_t grid;          /* CTAs launched                                                */
+  int32_t group_m;       /* rasterisation group height (tiles)                           */
+  int32_t smem_bytes;    /* dynamic shared memory per CTA                                */
+  int32_t tmem_cols;     /* tensor-memory columns allocated per CTA                      */
+  int64_t workspace_bytes; /* split-K partial sums + tickets                             */
+} hgemm_plan_t;
+
+/*
+ * hgemm_plan -- the launch plan hgemm_run would use for these arguments on a
+ * GPU with `num_sms` SMs (cluster capacity assumed num_sms / 2 pairs).
+ * `variant` = HGEMM_VARIANT_AUTO or a forced variant.  Validates the sizes,
+ * dtypes and layout like hgemm_run (pointers are not involved).
+ */
+hgemm_status_t hgemm_plan(int64_t M, int64_t N, int64_t K, hgemm_layout_t layout, hgemm_dtype_t in_dtype,
+                          hgemm_dtype_t acc_dtype, hgemm_dtype_t out_dtype, int32_t num_sms, int32_t variant,
+                          int32_t group_m, hgemm_plan_t* plan);
+
+/*
+ * hgemm_plan_tile -- the persistent scheduler's map from a linear tile index
+ * (0 <= t < plan->num_tiles) to tile coordinates: grouped rasterisation,
+ * group_m tile rows swept together along N.  The same function runs on the
+ * device.  For split-K plans, tile t is the t-th block of 128 rows of N.
+ */
+hgemm_status_t hgemm_plan_tile(const hgemm_plan_t* plan, int32_t t, int32_t* tile_m_idx, int32_t* tile_n_idx);
+
+/*
+ * hgemm_plan_splitk_range -- for a split-K plan, the contiguous range of
+ * (tile, k-block) work units that CTA `cta` owns: units [*begin, *end) of the
+ * tile-major linear order (unit u = tile * k_blocks + kb).
+ */
+hgemm_status_t hgemm_plan_splitk_range(const hgemm_plan_t* plan, int32_t cta, int64_t* begin, int64_t* end);
+
+/*
+ * hgemm_encode_idesc -- the 32-bit tcgen05.mma instruction descriptor the
+ * kernels use (kind::f16: D format bit 4-5, A/B format bits 7-9/10-12,
+ * A/B major bits 15/16, N>>3 at bit 17, M>>4 at bit 24).
+ */
+uint32_t hgemm_encode_idesc(int32_t mma_m, int32_t mma_n, hgemm_dtype_t in_dtype, hgemm_dtype_t acc_dtype,
+                            int32_t a_mn_major, int32_t b_mn_major);
+
+/*
+ * hgemm_encode_smem_desc -- the 64-bit shared-memory matrix descriptor
+ * (start address >> 4 at bits 0-13, leading byte offset >> 4 at 16-29, stride
+ * byte offset >> 4 at 32-45, version 1 at bit 46, swizzle mode at 61-63 with
+ * 2 = 128-byte swizzle).
+ */
+uint64_t hgemm_encode_smem_desc(uint32_t smem_addr, uint32_t lbo_bytes, uint32_t sbo_bytes, int32_t swizzle_mode);
+
+/* Library version, e.g. 100 for 0.1.0. */
+int32_t hgemm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HGEMM_H_ */

@@ -1,0 +1,483 @@
+// api.cu -- the C ABI declared in include/hgemm.h: argument validation, launch
+// planning, TMA tensor-map encoding and kernel dispatch (host code).
+//
+// Tensor maps follow "tcgen05 for dummies: a B200 GEMM from scratch"
+// (translated), section "TMA and mbarrier" (cuTensorMapEncodeTiled, dims and
+// strides innermost first, strides in bytes) and section "128-byte global
+// loads and swizzle" (64-element inner box with CU_TENSOR_MAP_SWIZZLE_128B).
+// The driver entry point is fetched through the runtime, so the library has no
+// link-time dependency on the driver and loads on machines without a GPU.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+#include <new>
+
+#include "../../include/hgemm.h"
+#include "desc.cuh"
+#include "kernels.h"
+#include "sched.cuh"
+
+using namespace hg;
+
+namespace {
+
+constexpr int32_t kVersion = 100;
+constexpr int kDefaultGroupM = 8;
+constexpr int kDefaultSmemOptin = 232448;  // 227 KiB, sm_100-class parts
+constexpr int64_t kMaxDim = 2147483647;
+
+struct Ctx {
+  int device = 0;
+  int sm_count = 0;
+  int smem_optin = 0;
+  int32_t* status = nullptr;  // device status word
+  float* partials = nullptr;  // split-K fp32 partial sums
+  size_t partials_bytes = 0;
+  int32_t* tickets = nullptr;  // split-K per-tile tickets, all zero between launches
+  size_t ticket_count = 0;
+  bool tickets_dirty = false;  // a launch gave up and may have left tickets behind
+  int force_variant = HGEMM_VARIANT_AUTO;
+  uint64_t timeout_ns = kDefaultTimeoutNs;
+  int inject = 0;
+  int group_m = kDefaultGroupM;
+  int max_ctas = 0;
+  int capacity[3] = {0, 0, 0};  // resident clusters per dense kind
+  int splitk_prepared_smem = 0;
+};
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+void load_encode() {
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+}
+
+bool valid_dtype(int d) { return d == HGEMM_F16 || d == HGEMM_BF16 || d == HGEMM_F32; }
+
+// Checks that do not involve pointers.  Order: sizes, enums, combinations, pitches.
+hgemm_status_t check_problem(int64_t M, int64_t N, int64_t K, int layout, int in, int acc, int out) {
+  if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return HGEMM_ERR_INVALID_ARG;
+  if (layout != HGEMM_LAYOUT_TN && layout != HGEMM_LAYOUT_NN) return HGEMM_ERR_INVALID_ARG;
+  if (!valid_dtype(in) || !valid_dtype(acc) || !valid_dtype(out)) return HGEMM_ERR_INVALID_ARG;
+  if (in == HGEMM_F32 || out == HGEMM_F32) return HGEMM_ERR_UNSUPPORTED;
+  if (acc == HGEMM_BF16) return HGEMM_ERR_UNSUPPORTED;
+  if (acc == HGEMM_F16 && in != HGEMM_F16) return HGEMM_ERR_UNSUPPORTED;
+  if (M == 0 || N == 0) return HGEMM_OK;
+  if (N % 8 != 0) return HGEMM_ERR_MISALIGNED;           // C (and NN B) row pitch
+  if (K > 0 && K % 8 != 0) return HGEMM_ERR_MISALIGNED;  // A (and TN B) row pitch
+  return HGEMM_OK;
+}
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+DenseKind kind_of(int variant) {
+  switch (variant) {
+    case HGEMM_VARIANT_1SM_128x128: return kDense1Sm128;
+    case HGEMM_VARIANT_1SM_128x256: return kDense1Sm256;
+    default: return kDense2Sm256;
+  }
+}
+
+int variant_of(DenseKind k) {
+  switch (k) {
+    case kDense1Sm128: return HGEMM_VARIANT_1SM_128x128;
+    case kDense1Sm256: return HGEMM_VARIANT_1SM_128x256;
+    default: return HGEMM_VARIANT_2SM_256x256;
+  }
+}
+
+void fill_dense_plan(DenseKind kind, int64_t M, int64_t N, int64_t K, int capacity, int group_m, int max_ctas,
+                     hgemm_plan_t* p) {
+  const DenseKindInfo info = dense_kind_info(kind);
+  p->variant = variant_of(kind);
+  p->cta_group = info.cta_group;
+  p->tile_m = 128 * info.cta_group;
+  p->tile_n = info.block_n;
+  p->block_k = 64;
+  p->stages = info.stages;
+  p->tiles_m = (int32_t)cdiv(M, p->tile_m);
+  p->tiles_n = (int32_t)cdiv(N, p->tile_n);
+  p->num_tiles = p->tiles_m * p->tiles_n;
+  p->k_blocks = (int32_t)cdiv(K, 64);
+  int clusters = capacity > 0 ? capacity : 1;
+  if (max_ctas > 0) {
+    int cap = max_ctas / info.cta_group;
+    if (cap < 1) cap = 1;
+    if (cap < clusters) clusters = cap;
+  }
+  if (p->num_tiles < clusters) clusters = p->num_tiles;
+  p->grid = clusters * info.cta_group;
+  p->group_m = group_m > 0 ? group_m : kDefaultGroupM;
+  p->smem_bytes = info.smem_bytes;
+  p->tmem_cols = info.tmem_cols;
+  p->workspace_bytes = 0;
+}
+
+// Estimated relative cost of a dense plan: waves of tiles x tile work / efficiency.
+double dense_cost(DenseKind kind, int64_t M, int64_t N, int capacity) {
+  const DenseKindInfo info = dense_kind_info(kind);
+  const int64_t tm = 128 * info.cta_group, tn = info.block_n;
+  const int64_t tiles = cdiv(M, tm) * cdiv(N, tn);
+  const int64_t slots = capacity > 0 ? capacity : 1;
+  const int64_t waves = cdiv(tiles, slots);
+  const double eff = (kind == kDense2Sm256) ? 1.0 : (kind == kDense1Sm256 ? 0.85 : 0.70);
+  // one wave of the whole chip does `slots` tiles, each (tm x tn) / per-SM share
+  return (double)waves * (double)(tm * tn) / (double)info.cta_group / eff;
+}
+
+hgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int layout, int in, int acc, int out, int num_sms,
+                         int smem_optin, const int capacity_in[3], int variant, int group_m, int max_ctas,
+                         hgemm_plan_t* p) {
+  memset(p, 0, sizeof(*p));
+  hgemm_status_t st = check_problem(M, N, K, layout, in, acc, out);
+  if (st != HGEMM_OK) return st;
+  if (num_sms <= 0) return HGEMM_ERR_INVALID_ARG;
+  if (variant < HGEMM_VARIANT_AUTO || variant > HGEMM_VARIANT_SPLITK) return HGEMM_ERR_INVALID_ARG;
+  int capacity[3];
+  for (int i = 0; i < 3; ++i) {
+    const DenseKindInfo info = dense_kind_info((DenseKind)i);
+    capacity[i] = (capacity_in && capacity_in[i] > 0) ? capacity_in[i] : num_sms / info.cta_group;
+  }
+  const bool splitk_ok = (M >= 1 && M <= kSplitKMaxM && layout == HGEMM_LAYOUT_TN && acc == HGEMM_F32);
+  if (variant == HGEMM_VARIANT_SPLITK && !splitk_ok) return HGEMM_ERR_UNSUPPORTED;
+  if (M == 0 || N == 0 || K == 0) {
+    p->variant = variant == HGEMM_VARIANT_AUTO ? HGEMM_VARIANT_1SM_128x128 : variant;
+    p->group_m = group_m > 0 ? group_m : kDefaultGroupM;
+    return HGEMM_OK;  // nothing or a zero fill to launch
+  }
+  if (variant == HGEMM_VARIANT_SPLITK || (variant == HGEMM_VARIANT_AUTO && splitk_ok)) {
+    const int mma_n = (int)cdiv(M, 16) * 16;
+    p->variant = HGEMM_VARIANT_SPLITK;
+    p->cta_group = 1;
+    p->tile_m = 128;
+    p->tile_n = mma_n;
+    p->block_k = 64;
+    p->stages = splitk_stages_for(mma_n, smem_optin > 0 ? smem_optin : kDefaultSmemOptin);
+    p->tiles_m = (int32_t)cdiv(N, 128);
+    p->tiles_n = 1;
+    p->num_tiles = p->tiles_m;
+    p->k_blocks = (int32_t)cdiv(K, 64);
+    const int64_t units = (int64_t)p->num_tiles * p->k_blocks;
+    int64_t grid = num_sms;
+    if (max_ctas > 0 && max_ctas < grid) grid = max_ctas;
+    if (units < grid) grid = units;
+    p->grid = (int32_t)grid;
+    p->group_m = 1;
+    p->smem_bytes = splitk_smem_bytes(mma_n, p->stages);
+    p->tmem_cols = splitk_tmem_cols(mma_n);
+    p->workspace_bytes = (int64_t)splitk_workspace_bytes(p->grid, mma_n, p->num_tiles);
+    return HGEMM_OK;
+  }
+  DenseKind kind;
+  if (variant != HGEMM_VARIANT_AUTO) {
+    kind = kind_of(variant);
+  } else {
+    kind = kDense2Sm256;
+    double best = dense_cost(kDense2Sm256, M, N, capacity[kDense2Sm256]);
+    for (DenseKind k : {kDense1Sm256, kDense1Sm128}) {
+      const double c = dense_cost(k, M, N, capacity[k]);
+      if (c < best) {
+        best = c;
+        kind = k;
+      }
+    }
+  }
+  fill_dense_plan(kind, M, N, K, capacity[kind], group_m, max_ctas, p);
+  return HGEMM_OK;
+}
+
+bool encode_2d(CUtensorMap* m, int dtype, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_inner,
+               uint32_t box_outer) {
+  if (!g_encode) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {inner * 2};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapDataType t =
+      dtype == HGEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  return g_encode(m, t, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool overlaps(uintptr_t a, size_t an, uintptr_t b, size_t bn) { return an > 0 && bn > 0 && a < b + bn && b < a + an; }
+
+hgemm_status_t cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return HGEMM_OK;
+  if (e == cudaErrorMemoryAllocation) return HGEMM_ERR_OOM;
+  if (e == cudaErrorNoDevice || e == cudaErrorInsufficientDriver) return HGEMM_ERR_NO_DEVICE;
+  return HGEMM_ERR_CUDA;
+}
+
+hgemm_status_t ensure_splitk_workspace(Ctx* c, size_t partial_bytes, size_t n_tiles, cudaStream_t s) {
+  if (c->partials_bytes < partial_bytes) {
+    if (c->partials) cudaFree(c->partials);
+    c->partials = nullptr;
+    c->partials_bytes = 0;
+    if (cudaMalloc(reinterpret_cast<void**>(&c->partials), partial_bytes) != cudaSuccess) return HGEMM_ERR_OOM;
+    c->partials_bytes = partial_bytes;
+  }
+  if (c->ticket_count < n_tiles) {
+    if (c->tickets) cudaFree(c->tickets);
+    c->tickets = nullptr;
+    c->ticket_count = 0;
+    const size_t count = (n_tiles + 3) & ~(size_t)3;  // whole 16-byte groups for the zero fill
+    if (cudaMalloc(reinterpret_cast<void**>(&c->tickets), count * sizeof(int32_t)) != cudaSuccess)
+      return HGEMM_ERR_OOM;
+    c->ticket_count = count;
+    c->tickets_dirty = true;
+  }
+  if (c->tickets_dirty) {
+    cudaError_t e = fill_zero_launch(c->tickets, c->ticket_count * sizeof(int32_t), s);
+    if (e != cudaSuccess) return cuda_status(e);
+    c->tickets_dirty = false;
+  }
+  return HGEMM_OK;
+}
+
+}  // namespace
+
+struct hgemm_ctx : Ctx {};
+
+extern "C" {
+
+const char* hgemm_status_string(hgemm_status_t s) {
+  switch (s) {
+    case HGEMM_OK: return "HGEMM_OK";
+    case HGEMM_ERR_INVALID_ARG: return "HGEMM_ERR_INVALID_ARG: invalid argument";
+    case HGEMM_ERR_UNSUPPORTED: return "HGEMM_ERR_UNSUPPORTED: unsupported combination or device";
+    case HGEMM_ERR_MISALIGNED: return "HGEMM_ERR_MISALIGNED: pointer or row pitch not 16-byte aligned";
+    case HGEMM_ERR_ALIAS: return "HGEMM_ERR_ALIAS: C overlaps A or B";
+    case HGEMM_ERR_NO_DEVICE: return "HGEMM_ERR_NO_DEVICE: no usable CUDA device";
+    case HGEMM_ERR_CUDA: return "HGEMM_ERR_CUDA: a CUDA call failed";
+    case HGEMM_ERR_TIMEOUT: return "HGEMM_ERR_TIMEOUT: a device-side wait gave up";
+    case HGEMM_ERR_OOM: return "HGEMM_ERR_OOM: device allocation failed";
+  }
+  return "unknown hgemm status";
+}
+
+int32_t hgemm_version(void) { return kVersion; }
+
+uint32_t hgemm_encode_idesc(int32_t mma_m, int32_t mma_n, hgemm_dtype_t in_dtype, hgemm_dtype_t acc_dtype,
+                            int32_t a_mn_major, int32_t b_mn_major) {
+  return make_idesc(mma_m, mma_n, in_dtype == HGEMM_BF16, acc_dtype == HGEMM_F32, a_mn_major != 0, b_mn_major != 0);
+}
+
+uint64_t hgemm_encode_smem_desc(uint32_t smem_addr, uint32_t lbo_bytes, uint32_t sbo_bytes, int32_t swizzle_mode) {
+  return make_smem_desc(smem_addr, lbo_bytes, sbo_bytes, swizzle_mode);
+}
+
+hgemm_status_t hgemm_plan(int64_t M, int64_t N, int64_t K, hgemm_layout_t layout, hgemm_dtype_t in_dtype,
+                          hgemm_dtype_t acc_dtype, hgemm_dtype_t out_dtype, int32_t num_sms, int32_t variant,
+                          int32_t group_m, hgemm_plan_t* plan) {
+  if (!plan) return HGEMM_ERR_INVALID_ARG;
+  return make_plan(M, N, K, layout, in_dtype, acc_dtype, out_dtype, num_sms, kDefaultSmemOptin, nullptr, variant,
+                   group_m, 0, plan);
+}
+
+hgemm_status_t hgemm_plan_tile(const hgemm_plan_t* plan, int32_t t, int32_t* tile_m_idx, int32_t* tile_n_idx) {
+  if (!plan || !tile_m_idx || !tile_n_idx || t < 0 || t >= plan->num_tiles || plan->group_m <= 0)
+    return HGEMM_ERR_INVALID_ARG;
+  const TileCoord c = tile_coord(t, plan->tiles_m, plan->tiles_n, plan->group_m);
+  *tile_m_idx = c.m;
+  *tile_n_idx = c.n;
+  return HGEMM_OK;
+}
+
+hgemm_status_t hgemm_plan_splitk_range(const hgemm_plan_t* plan, int32_t cta, int64_t* begin, int64_t* end) {
+  if (!plan || !begin || !end || plan->variant != HGEMM_VARIANT_SPLITK || cta < 0 || cta >= plan->grid)
+    return HGEMM_ERR_INVALID_ARG;
+  const int64_t units = (int64_t)plan->num_tiles * plan->k_blocks;
+  *begin = splitk_begin(cta, units, plan->grid);
+  *end = splitk_begin((int64_t)cta + 1, units, plan->grid);
+  return HGEMM_OK;
+}
+
+hgemm_status_t hgemm_create(hgemm_handle_t* out) {
+  if (!out) return HGEMM_ERR_INVALID_ARG;
+  *out = nullptr;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return HGEMM_ERR_NO_DEVICE;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return HGEMM_ERR_NO_DEVICE;
+  if (major != 10 || minor != 3) return HGEMM_ERR_UNSUPPORTED;
+  std::call_once(g_encode_once, load_encode);
+  if (!g_encode) return HGEMM_ERR_NO_DEVICE;
+  hgemm_ctx* c = new (std::nothrow) hgemm_ctx();
+  if (!c) return HGEMM_ERR_OOM;
+  c->device = dev;
+  if (cudaDeviceGetAttribute(&c->sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&c->smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
+    delete c;
+    return HGEMM_ERR_CUDA;
+  }
+  e = cudaMalloc(&c->status, 16);
+  if (e == cudaSuccess) e = cudaMemset(c->status, 0, 16);
+  for (int k = 0; e == cudaSuccess && k < 3; ++k) {
+    e = dense_prepare((DenseKind)k);
+    if (e == cudaSuccess) e = dense_max_active_clusters((DenseKind)k, &c->capacity[k]);
+  }
+  if (e == cudaSuccess) {
+    e = splitk_prepare(c->smem_optin);
+    c->splitk_prepared_smem = c->smem_optin;
+  }
+  if (e != cudaSuccess) {
+    if (c->status) cudaFree(c->status);
+    delete c;
+    return cuda_status(e);
+  }
+  *out = c;
+  return HGEMM_OK;
+}
+
+hgemm_status_t hgemm_destroy(hgemm_handle_t h) {
+  if (!h) return HGEMM_OK;
+  int prev = 0;
+  cudaGetDevice(&prev);
+  cudaSetDevice(h->device);
+  cudaError_t e = cudaDeviceSynchronize();
+  if (h->partials) cudaFree(h->partials);
+  if (h->tickets) cudaFree(h->tickets);
+  if (h->status) cudaFree(h->status);
+  cudaSetDevice(prev);
+  delete h;
+  return e == cudaSuccess ? HGEMM_OK : HGEMM_ERR_CUDA;
+}
+
+hgemm_status_t hgemm_set_option(hgemm_handle_t h, int32_t option, int64_t value) {
+  if (!h) return HGEMM_ERR_INVALID_ARG;
+  switch (option) {
+    case HGEMM_OPT_FORCE_VARIANT:
+      if (value < HGEMM_VARIANT_AUTO || value > HGEMM_VARIANT_SPLITK) return HGEMM_ERR_INVALID_ARG;
+      h->force_variant = (int)value;
+      return HGEMM_OK;
+    case HGEMM_OPT_TIMEOUT_NS:
+      if (value <= 0) return HGEMM_ERR_INVALID_ARG;
+      h->timeout_ns = (uint64_t)value;
+      return HGEMM_OK;
+    case HGEMM_OPT_INJECT_FAULT:
+      if (value < 0 || value > 1) return HGEMM_ERR_INVALID_ARG;
+      h->inject = (int)value;
+      return HGEMM_OK;
+    case HGEMM_OPT_GROUP_M:
+      if (value < 1 || value > 65536) return HGEMM_ERR_INVALID_ARG;
+      h->group_m = (int)value;
+      return HGEMM_OK;
+    case HGEMM_OPT_MAX_CTAS:
+      if (value < 0 || value > 65536) return HGEMM_ERR_INVALID_ARG;
+      h->max_ctas = (int)value;
+      return HGEMM_OK;
+  }
+  return HGEMM_ERR_INVALID_ARG;
+}
+
+hgemm_status_t hgemm_run(hgemm_handle_t h, const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                         hgemm_layout_t layout, hgemm_dtype_t in_dtype, hgemm_dtype_t acc_dtype,
+                         hgemm_dtype_t out_dtype, void* stream) {
+  if (!h) return HGEMM_ERR_INVALID_ARG;
+  hgemm_status_t st = check_problem(M, N, K, layout, in_dtype, acc_dtype, out_dtype);
+  if (st != HGEMM_OK) return st;
+  if (M == 0 || N == 0) return HGEMM_OK;
+  if (!C || (K > 0 && (!A || !B))) return HGEMM_ERR_INVALID_ARG;
+  const uintptr_t a = reinterpret_cast<uintptr_t>(A), b = reinterpret_cast<uintptr_t>(B),
+                  c = reinterpret_cast<uintptr_t>(C);
+  if ((c & 15u) != 0 || (K > 0 && ((a & 15u) != 0 || (b & 15u) != 0))) return HGEMM_ERR_MISALIGNED;
+  const size_t a_bytes = (size_t)M * (size_t)K * 2, b_bytes = (size_t)K * (size_t)N * 2,
+               c_bytes = (size_t)M * (size_t)N * 2;
+  if (overlaps(c, c_bytes, a, a_bytes) || overlaps(c, c_bytes, b, b_bytes)) return HGEMM_ERR_ALIAS;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (K == 0) return cuda_status(fill_zero_launch(C, c_bytes, s));
+
+  hgemm_plan_t p;
+  st = make_plan(M, N, K, layout, in_dtype, acc_dtype, out_dtype, h->sm_count, h->smem_optin, h->capacity,
+                 h->force_variant, h->group_m, h->max_ctas, &p);
+  if (st != HGEMM_OK) return st;
+
+  if (p.variant == HGEMM_VARIANT_SPLITK) {
+    const int mma_n = p.tile_n;
+    CUtensorMap tmW, tmX;
+    if (!encode_2d(&tmW, in_dtype, B, (uint64_t)K, (uint64_t)N, 64, 128) ||
+        !encode_2d(&tmX, in_dtype, A, (uint64_t)K, (uint64_t)M, 64, (uint32_t)mma_n))
+      return HGEMM_ERR_CUDA;
+    const size_t partial_bytes = (size_t)p.grid * 2 * 128 * (size_t)mma_n * sizeof(float);
+    st = ensure_splitk_workspace(h, partial_bytes, (size_t)p.num_tiles, s);
+    if (st != HGEMM_OK) return st;
+    if (p.smem_bytes > h->splitk_prepared_smem) return HGEMM_ERR_UNSUPPORTED;
+    SplitKArgs args;
+    args.M = (int32_t)M;
+    args.N = (int32_t)N;
+    args.K = (int32_t)K;
+    args.mma_n = mma_n;
+    args.n_tiles = p.num_tiles;
+    args.k_blocks = p.k_blocks;
+    args.units = (int64_t)p.num_tiles * p.k_blocks;
+    args.stages = p.stages;
+    args.idesc = make_idesc(128, mma_n, in_dtype == HGEMM_BF16, true, false, false);
+    args.out_bf16 = out_dtype == HGEMM_BF16;
+    args.inject = h->inject;
+    args.timeout_ns = h->timeout_ns;
+    args.status = h->status;
+    args.partials = h->partials;
+    args.tickets = h->tickets;
+    args.C = C;
+    return cuda_status(splitk_launch(tmW, tmX, args, p.grid, p.smem_bytes, s));
+  }
+
+  const DenseKind kind = kind_of(p.variant);
+  const DenseKindInfo info = dense_kind_info(kind);
+  const bool nn = layout == HGEMM_LAYOUT_NN;
+  CUtensorMap tmA, tmB, tmC;
+  bool ok = encode_2d(&tmA, in_dtype, A, (uint64_t)K, (uint64_t)M, 64, 128);
+  if (!nn)
+    ok = ok && encode_2d(&tmB, in_dtype, B, (uint64_t)K, (uint64_t)N, 64, (uint32_t)(info.block_n / info.cta_group));
+  else
+    ok = ok && encode_2d(&tmB, in_dtype, B, (uint64_t)N, (uint64_t)K, 64, 64);
+  ok = ok && encode_2d(&tmC, out_dtype, C, (uint64_t)N, (uint64_t)M, 64, 32);
+  if (!ok) return HGEMM_ERR_CUDA;
+  DenseArgs args;
+  args.M = (int32_t)M;
+  args.N = (int32_t)N;
+  args.K = (int32_t)K;
+  args.tiles_m = p.tiles_m;
+  args.tiles_n = p.tiles_n;
+  args.num_tiles = p.num_tiles;
+  args.k_blocks = p.k_blocks;
+  args.group_m = p.group_m;
+  args.idesc = make_idesc(128 * info.cta_group, info.block_n, in_dtype == HGEMM_BF16, acc_dtype == HGEMM_F32, false, nn);
+  args.b_mn_major = nn ? 1 : 0;
+  args.acc_f16 = acc_dtype == HGEMM_F16;
+  args.out_bf16 = out_dtype == HGEMM_BF16;
+  args.inject = h->inject;
+  args.timeout_ns = h->timeout_ns;
+  args.status = h->status;
+  return cuda_status(dense_launch(kind, tmA, tmB, tmC, args, p.grid, s));
+}
+
+hgemm_status_t hgemm_sync_status(hgemm_handle_t h, void* stream, int32_t* detail) {
+  if (!h) return HGEMM_ERR_INVALID_ARG;
+  if (detail) *detail = 0;
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_status(e);
+  int32_t word = 0;
+  e = cudaMemcpy(&word, h->status, sizeof(word), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_status(e);
+  if (detail) *detail = word;
+  if (word == 0) return HGEMM_OK;
+  e = cudaMemset(h->status, 0, sizeof(int32_t));
+  if (e != cudaSuccess) return cuda_status(e);
+  h->tickets_dirty = true;  // a split-K launch that gave up may leave tickets behind
+  return (hgemm_status_t)(word & 0xFF);
+}
+
+}  // extern "C"

@@ -1,0 +1,457 @@
+// gemm_dense.cu -- persistent, warp-specialised tcgen05 GEMM for sm_103a.
+//
+// C[M,N] = A[M,K] . B[K,N], fp16/bf16 inputs, fp32 or fp16 accumulators in
+// tensor memory, fp16/bf16 output.  The kernel structure follows the steps of
+// "tcgen05 for dummies: a B200 GEMM from scratch" (translated):
+//   - "TMA and mbarrier": tiles move global -> shared with cp.async.bulk.tensor,
+//     completion tracked by transaction-count mbarriers;
+//   - "128-byte global loads and swizzle": 64-element (128 B) boxes with the
+//     128-byte swizzle, matched by the MMA's shared-memory descriptor;
+//   - "Pipelining" and "Warp specialization": a STAGES-deep ring with full /
+//     empty barrier pairs, one TMA warp, one MMA warp;
+//   - "2-SM MMA": cta_group::2, a CTA pair computes a 256-row tile, each CTA
+//     loads its own 128 rows of A and half of the B tile;
+//   - "Persistent kernel: static scheduling": one CTA (pair) per SM walks its
+//     tiles; tensor-memory accumulators are double-buffered so the epilogue of
+//     one tile overlaps the mainloop of the next.
+// Differences from the page: the epilogue goes tcgen05.ld -> cast -> swizzled
+// shared staging -> TMA store (the page stored from registers); tiles are
+// visited in grouped (L2-friendly) order; every wait is bounded and a wait
+// that gives up reports HGEMM_ERR_TIMEOUT instead of hanging; ragged M, N and
+// K are handled by TMA zero fill on loads and clipping on stores; NN layout
+// (B row-major, MN-major operand) and fp16 accumulation are supported.
+//
+// Warp roles (192 threads):
+//   warp 0      TMA producer (one thread)
+//   warp 1      TMEM allocator; MMA issuer (one thread; in a CTA pair only CTA 0)
+//   warps 2..5  epilogue; warp w reads TMEM lanes 32*(w%4) .. 32*(w%4)+31
+#include <cuda_fp16.h>
+
+#include "desc.cuh"
+#include "kernels.h"
+#include "ptx.cuh"
+#include "sched.cuh"
+
+namespace hg {
+
+template <int CG, int BN, int STAGES>
+struct DenseShape {
+  static constexpr int BM = 128;                  // C rows per CTA
+  static constexpr int BK = 64;                   // K elements per stage: one 128 B swizzle row
+  static constexpr int A_BYTES = BM * BK * 2;     // 16 KiB
+  static constexpr int B_ROWS = BN / CG;          // N extent of the B slice this CTA loads
+  static constexpr int B_BYTES = B_ROWS * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int EPI_BOX_COLS = 64;         // output columns per TMA store box (128 B)
+  static constexpr int EPI_BOX_BYTES = 32 * 128;  // 32 rows x 128 B
+  static constexpr int EPI_BYTES = 4 * 2 * EPI_BOX_BYTES;  // 4 warps x double buffer
+  static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
+  static constexpr int BAR_OFF = RING_BYTES + EPI_BYTES;
+  static constexpr int NUM_BARS = 2 * STAGES + 5;  // full[S], empty[S], tmem_full[2], tmem_empty[2], drain
+  static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
+  static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + alignment slack for the 1 KiB base
+  static constexpr int TMEM_COLS = 2 * BN;
+  static constexpr int THREADS = 192;
+  static_assert(BN % 64 == 0 && BN <= 256, "BN");
+  static_assert((BN / CG) % 64 == 0, "B slice must be whole 64-column boxes");
+  static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation must be a power of two");
+  static_assert(SMEM_BYTES <= 232448, "shared memory");
+};
+
+__device__ __forceinline__ void report_timeout(int32_t* status, int32_t role, volatile uint32_t* abort_flag) {
+  *abort_flag = 1u;
+  atomicCAS(status, 0, kStatusTimeout | (role << 8) | ((int32_t)(blockIdx.x & 0xFFFF) << 16));
+}
+
+// fp16x2 (packed) -> the output's packed pair.
+__device__ __forceinline__ uint32_t f16x2_to_out(uint32_t h2, bool out_bf16) {
+  if (!out_bf16) return h2;
+  __half2 h = *reinterpret_cast<__half2*>(&h2);
+  float2 f = __half22float2(h);
+  return pack_f32x2_to_bf16x2(f.x, f.y);
+}
+
+template <int CG, int BN, int STAGES>
+__global__ void __launch_bounds__(192, 1)
+    dense_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                      const __grid_constant__ CUtensorMap tmC, const DenseArgs args) {
+  using S = DenseShape<CG, BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;  // 128 B swizzle atoms need 1 KiB alignment
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t ring = base;
+  const uint32_t epi = base + S::RING_BYTES;
+  const uint32_t bars = base + S::BAR_OFF;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + S::MISC_OFF);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(gbase + S::MISC_OFF + 4);
+
+  auto full_bar = [&](int s) -> uint32_t { return bars + 8u * s; };
+  auto empty_bar = [&](int s) -> uint32_t { return bars + 8u * (STAGES + s); };
+  auto tfull_bar = [&](int b) -> uint32_t { return bars + 8u * (2 * STAGES + b); };
+  auto tempty_bar = [&](int b) -> uint32_t { return bars + 8u * (2 * STAGES + 2 + b); };
+  const uint32_t drain_bar = bars + 8u * (2 * STAGES + 4);
+
+  const int warp = threadIdx.x / 32;
+  const uint32_t lane = threadIdx.x % 32;
+  const uint32_t rank = (CG == 2) ? cluster_ctarank() : 0u;
+  const int cluster = (CG == 2) ? (int)cluster_id_x() : (int)blockIdx.x;
+  const int nclusters = (CG == 2) ? (int)num_clusters_x() : (int)gridDim.x;
+  constexpr bool kCS = (CG == 2);  // cluster-scope waits on barriers that see peer signals
+  const WaitCtl ctl{args.timeout_ns, abort_flag};
+  const WaitCtl drain_ctl{kDrainTimeoutNs, nullptr};
+
+  // ------------------------------------------------------------ setup ----
+  if (warp == 0) {
+    if (lane == 0) {
+      for (int s = 0; s < STAGES; ++s) {
+        mbar_init(full_bar(s), 1);
+        mbar_init(empty_bar(s), 1);
+      }
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(tfull_bar(b), 1);
+        mbar_init(tempty_bar(b), 4 * CG);  // every epilogue warp of the pair arrives
+      }
+      mbar_init(drain_bar, 1);
+      *abort_flag = 0u;
+      fence_mbar_init();
+      prefetch_tmap(&tmA);
+      prefetch_tmap(&tmB);
+      prefetch_tmap(&tmC);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    tmem_alloc<CG>(smem_addr(tmem_slot), S::TMEM_COLS);
+    tmem_relinquish<CG>();
+    tc_fence_before();
+  }
+  if constexpr (CG == 2)
+    cluster_sync();
+  else
+    __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+  bool aborted = false;
+
+  if (warp == 0) {
+    // ------------------------------------------------- TMA producer ----
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int64_t issued = 0;
+      bool ok = true;
+      const uint32_t full_rank0 = (CG == 2) ? mapa_shared(full_bar(0), 0) : full_bar(0);
+      for (int t = cluster; ok && t < args.num_tiles; t += nclusters) {
+        const TileCoord tc = tile_coord(t, args.tiles_m, args.tiles_n, args.group_m);
+        const int m_row = tc.m * (S::BM * CG) + (int)rank * S::BM;
+        const int n_row = tc.n * BN + (int)rank * S::B_ROWS;
+        for (int kb = 0; kb < args.k_blocks; ++kb) {
+          if (!mbar_wait<kCS>(empty_bar(stage), phase ^ 1u, ctl)) {
+            ok = false;
+            break;
+          }
+          const bool drop = (args.inject == 1) && (blockIdx.x == 0) && (issued == 0);
+          if (!drop) {
+            const uint32_t a_dst = ring + (uint32_t)stage * S::STAGE_BYTES;
+            const uint32_t b_dst = a_dst + S::A_BYTES;
+            const int k0 = kb * S::BK;
+            if constexpr (CG == 1) {
+              const uint32_t fb = full_bar(stage);
+              mbar_arrive_expect_tx(fb, S::STAGE_BYTES);
+              tma_load_2d(a_dst, &tmA, fb, k0, m_row);
+              if (!args.b_mn_major) {
+                tma_load_2d(b_dst, &tmB, fb, k0, n_row);
+              } else {
+#pragma unroll
+                for (int j = 0; j < S::B_ROWS / 64; ++j) tma_load_2d(b_dst + j * 8192, &tmB, fb, n_row + 64 * j, k0);
+              }
+            } else {
+              // Both CTAs report their bytes to CTA 0's barrier, which expects the pair's total.
+              const uint32_t fb = full_rank0 + 8u * (uint32_t)stage;
+              if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * S::STAGE_BYTES);
+              tma_load_2d_pair(a_dst, &tmA, fb, k0, m_row);
+              if (!args.b_mn_major) {
+                tma_load_2d_pair(b_dst, &tmB, fb, k0, n_row);
+              } else {
+#pragma unroll
+                for (int j = 0; j < S::B_ROWS / 64; ++j)
+                  tma_load_2d_pair(b_dst + j * 8192, &tmB, fb, n_row + 64 * j, k0);
+              }
+            }
+          }
+          ++issued;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        report_timeout(args.status, kRoleProducer, abort_flag);
+        aborted = true;
+      }
+      // Every load this CTA issued and signalled on its own barrier must land
+      // before the CTA can exit.  In the normal path these waits return at once.
+      if (CG == 1 || rank == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+          if (issued <= s) break;
+          const int64_t last = s + (int64_t)STAGES * ((issued - 1 - s) / STAGES);
+          const bool dropped = (args.inject == 1) && (blockIdx.x == 0) && (last == 0);
+          if (dropped) continue;
+          if (!mbar_wait<kCS>(full_bar(s), (uint32_t)((last / STAGES) & 1), drain_ctl)) {
+            report_timeout(args.status, kRoleTeardown, abort_flag);
+            aborted = true;
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // --------------------------------------------------- MMA issuer ----
+    if ((CG == 1 || rank == 0) && lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      const uint32_t b_step = args.b_mn_major ? (kMNMajorStepBytes >> 4) : (kKMajorStepBytes >> 4);
+      const uint32_t b_lbo = args.b_mn_major ? kMNMajorLBO : 16u;
+      const uint32_t b_sbo = args.b_mn_major ? kMNMajorSBO : kKMajorSBO;
+      for (int t = cluster; ok && t < args.num_tiles; t += nclusters) {
+        // Wait until the epilogue has drained this accumulator buffer.
+        if (!mbar_wait<kCS>(tempty_bar(acc), acc_phase ^ 1u, ctl)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        for (int kb = 0; kb < args.k_blocks; ++kb) {
+          if (!mbar_wait<kCS>(full_bar(stage), phase, ctl)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = ring + (uint32_t)stage * S::STAGE_BYTES;
+          const uint32_t b_addr = a_addr + S::A_BYTES;
+          const uint64_t a_desc = make_smem_desc(a_addr, 16u, kKMajorSBO, kSwizzle128B);
+          const uint64_t b_desc = make_smem_desc(b_addr, b_lbo, b_sbo, kSwizzle128B);
+#pragma unroll
+          for (int kk = 0; kk < S::BK / 16; ++kk) {
+            mma_f16<CG>(d_tmem, a_desc + (uint64_t)(kk * (kKMajorStepBytes >> 4)), b_desc + (uint64_t)(kk * b_step),
+                        args.idesc, (uint32_t)((kb | kk) != 0));
+          }
+          tc_commit_cg<CG>(empty_bar(stage), (uint16_t)0x3);  // frees the stage once these MMAs finish
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit_cg<CG>(tfull_bar(acc), (uint16_t)0x3);  // accumulator ready for the epilogue
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      if (!ok) {
+        report_timeout(args.status, kRoleMma, abort_flag);
+        aborted = true;
+      }
+      // Drain: every MMA issued above completes before tensor memory is released.
+      tc_commit_cg<CG>(drain_bar, (uint16_t)0x1);
+      if (!mbar_wait<false>(drain_bar, 0u, WaitCtl{args.timeout_ns, nullptr})) {
+        report_timeout(args.status, kRoleTeardown, abort_flag);
+        aborted = true;
+      }
+    }
+    __syncwarp();
+  } else {
+    // ----------------------------------------------------- epilogue ----
+    const int q = warp & 3;   // TMEM lane quarter this warp may access
+    const int ew = warp - 2;  // staging slot
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    uint32_t nstores = 0;
+    bool ok = true;
+    const bool out_bf16 = args.out_bf16 != 0;
+    for (int t = cluster; t < args.num_tiles; t += nclusters) {
+      bool got = mbar_wait<kCS>(tfull_bar(acc), acc_phase, ctl);
+      got = __all_sync(0xffffffffu, got);
+      if (!got) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const TileCoord tc = tile_coord(t, args.tiles_m, args.tiles_n, args.group_m);
+      const int m0 = tc.m * (S::BM * CG) + (int)rank * S::BM + q * 32;  // first C row of this warp
+      const int n0 = tc.n * BN;
+      const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+#pragma unroll 1
+      for (int c = 0; c < BN / 64; ++c) {
+        uint32_t p[32];
+        if (!args.acc_f16) {
+          uint32_t v[64];
+          tmem_ld_x32(t_row + (uint32_t)(c * 64), v);
+          tmem_ld_x32(t_row + (uint32_t)(c * 64 + 32), v + 32);
+          tmem_ld_wait();
+          if (out_bf16) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) p[i] = pack_f32x2_to_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) p[i] = pack_f32x2_to_f16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+          }
+        } else {
+          // fp16 accumulators occupy one 32-bit TMEM column each, in the low half.
+          uint32_t v[64];
+          tmem_ld_x32(t_row + (uint32_t)(c * 64), v);
+          tmem_ld_x32(t_row + (uint32_t)(c * 64 + 32), v + 32);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) p[i] = f16x2_to_out((v[2 * i] & 0xFFFFu) | (v[2 * i + 1] << 16), out_bf16);
+        }
+        if (c == BN / 64 - 1) {
+          // All reads of this accumulator are done: hand it back to the MMA warp.
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            if constexpr (CG == 1)
+              mbar_arrive(tempty_bar(acc));
+            else
+              mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));
+          }
+        }
+        const int nc = n0 + c * S::EPI_BOX_COLS;
+        if (m0 < args.M && nc < args.N) {  // warp-uniform; rows/cols past the edge are clipped by TMA
+          const uint32_t buf = epi + (uint32_t)(ew * 2 + (int)(nstores & 1u)) * S::EPI_BOX_BYTES;
+          if (lane == 0) bulk_wait_read<1>();  // the store that last used this buffer has read it
+          __syncwarp();
+          const uint32_t row = buf + lane * 128u;
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            st_shared_v4(row + ((uint32_t)(j ^ (int)(lane & 7u)) << 4), p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmC, buf, nc, m0);
+            bulk_commit();
+          }
+          ++nstores;
+        }
+      }
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+    if (!ok) {
+      if (lane == 0) report_timeout(args.status, kRoleEpilogue, abort_flag);
+      aborted = true;
+    }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+  }
+
+  // --------------------------------------------------------- teardown ----
+  if constexpr (CG == 2) {
+    // In a pair, the peer's loads signal CTA 0 and CTA 0's MMAs read the peer's
+    // shared memory; after a give-up, leave time for copies still in flight.
+    if (__syncthreads_or(aborted ? 1 : 0)) {
+      const uint64_t t0 = globaltimer_ns();
+      while (globaltimer_ns() - t0 < 50000ull) {
+      }
+    }
+    cluster_sync();
+  } else {
+    __syncthreads();
+  }
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc<CG>(tmem_base, S::TMEM_COLS);
+  }
+}
+
+// --------------------------------------------------------------- host ----
+#define HG_DENSE_KINDS(X) \
+  X(kDense1Sm128, 1, 128, 6) \
+  X(kDense1Sm256, 1, 256, 4) \
+  X(kDense2Sm256, 2, 256, 6)
+
+DenseKindInfo dense_kind_info(DenseKind kind) {
+  switch (kind) {
+#define X(KIND, CG, BN, ST)                                                                                 \
+  case KIND:                                                                                                \
+    return DenseKindInfo{CG, BN, ST, DenseShape<CG, BN, ST>::SMEM_BYTES, DenseShape<CG, BN, ST>::TMEM_COLS, \
+                         DenseShape<CG, BN, ST>::THREADS};
+    HG_DENSE_KINDS(X)
+#undef X
+  }
+  return DenseKindInfo{0, 0, 0, 0, 0, 0};
+}
+
+static const void* dense_fn(DenseKind kind) {
+  switch (kind) {
+#define X(KIND, CG, BN, ST) \
+  case KIND:                \
+    return reinterpret_cast<const void*>(&dense_gemm_kernel<CG, BN, ST>);
+    HG_DENSE_KINDS(X)
+#undef X
+  }
+  return nullptr;
+}
+
+cudaError_t dense_prepare(DenseKind kind) {
+  const DenseKindInfo info = dense_kind_info(kind);
+  const void* fn = dense_fn(kind);
+  if (!fn) return cudaErrorInvalidValue;
+  return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, info.smem_bytes);
+}
+
+static void fill_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, const DenseKindInfo& info, int grid,
+                        cudaStream_t stream) {
+  cfg = cudaLaunchConfig_t{};
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3((unsigned)info.threads, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)info.smem_bytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 0;
+  if (info.cta_group > 1) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)info.cta_group;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.numAttrs = 1;
+  }
+}
+
+cudaError_t dense_max_active_clusters(DenseKind kind, int* clusters) {
+  const DenseKindInfo info = dense_kind_info(kind);
+  if (info.cta_group == 1) {
+    int dev = 0, sms = 0, per_sm = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dense_fn(kind), info.threads, (size_t)info.smem_bytes);
+    *clusters = per_sm * sms;
+    return e;
+  }
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[1];
+  fill_config(cfg, attr, info, info.cta_group * 64, nullptr);
+  return cudaOccupancyMaxActiveClusters(clusters, dense_fn(kind), &cfg);
+}
+
+cudaError_t dense_launch(DenseKind kind, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
+                         const DenseArgs& args, int grid_ctas, cudaStream_t stream) {
+  const DenseKindInfo info = dense_kind_info(kind);
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[1];
+  fill_config(cfg, attr, info, grid_ctas, stream);
+  switch (kind) {
+#define X(KIND, CG, BN, ST) \
+  case KIND:                \
+    return cudaLaunchKernelEx(&cfg, dense_gemm_kernel<CG, BN, ST>, tmA, tmB, tmC, args);
+    HG_DENSE_KINDS(X)
+#undef X
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace hg

@@ -1,0 +1,77 @@
+// kernels.h -- internal interface between the C-ABI layer and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace hg {
+
+// Device status word layout (shared with hgemm_sync_status).
+constexpr int32_t kStatusTimeout = 7;  // == HGEMM_ERR_TIMEOUT
+enum Role : int32_t { kRoleProducer = 1, kRoleMma = 2, kRoleEpilogue = 3, kRoleTeardown = 4 };
+
+// Default limit of every bounded device-side wait.
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+// Limit used when draining in-flight copies after another role gave up.
+constexpr uint64_t kDrainTimeoutNs = 2000000ull;
+
+// ---------------------------------------------------------------- dense ----
+struct DenseArgs {
+  int32_t M, N, K;
+  int32_t tiles_m, tiles_n, num_tiles, k_blocks, group_m;
+  uint32_t idesc;
+  int32_t b_mn_major;      // NN layout: B tile is MN-major in shared memory
+  int32_t acc_f16;         // fp16 accumulators in tensor memory (one per 32-bit column, low half)
+  int32_t out_bf16;        // output dtype: 1 bf16, 0 fp16
+  int32_t inject;          // test-only fault injection (HGEMM_OPT_INJECT_FAULT)
+  uint64_t timeout_ns;
+  int32_t* status;
+};
+
+enum DenseKind : int { kDense1Sm128 = 0, kDense1Sm256 = 1, kDense2Sm256 = 2 };
+
+struct DenseKindInfo {
+  int cta_group, block_n, stages, smem_bytes, tmem_cols, threads;
+};
+DenseKindInfo dense_kind_info(DenseKind kind);
+
+// Sets the kernel attributes (dynamic shared memory) on the current device.
+cudaError_t dense_prepare(DenseKind kind);
+// Number of CTA clusters of this kernel that fit on the device at once.
+cudaError_t dense_max_active_clusters(DenseKind kind, int* clusters);
+cudaError_t dense_launch(DenseKind kind, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
+                         const DenseArgs& args, int grid_ctas, cudaStream_t stream);
+
+// ---------------------------------------------------------------- split-K ----
+struct SplitKArgs {
+  int32_t M, N, K;
+  int32_t mma_n;     // M rounded up to a multiple of 16 (the MMA's N)
+  int32_t n_tiles;   // ceil(N / 128)
+  int32_t k_blocks;  // ceil(K / 64)
+  int64_t units;     // n_tiles * k_blocks
+  int32_t stages;
+  uint32_t idesc;
+  int32_t out_bf16;
+  int32_t inject;
+  uint64_t timeout_ns;
+  int32_t* status;
+  float* partials;   // [grid][2][128][mma_n] fp32
+  int32_t* tickets;  // [n_tiles], all zero between launches
+  void* C;           // [M][N] row-major
+};
+
+constexpr int kSplitKMaxM = 64;
+int splitk_stage_bytes(int mma_n);
+int splitk_smem_bytes(int mma_n, int stages);
+int splitk_stages_for(int mma_n, int smem_optin);
+int splitk_tmem_cols(int mma_n);
+size_t splitk_workspace_bytes(int grid, int mma_n, int n_tiles);
+cudaError_t splitk_prepare(int smem_bytes);
+cudaError_t splitk_launch(const CUtensorMap& tmW, const CUtensorMap& tmX, const SplitKArgs& args, int grid,
+                          int smem_bytes, cudaStream_t stream);
+
+// ---------------------------------------------------------------- misc ----
+cudaError_t fill_zero_launch(void* p, size_t bytes, cudaStream_t stream);
+
+}  // namespace hg

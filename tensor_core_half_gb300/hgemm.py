@@ -1,0 +1,273 @@
+"""Python binding of the C ABI in include/hgemm.h (ctypes; marshalling only).
+
+Every function here converts Python arguments to the C types and calls the
+entry point of the same name in libhgemm.so; all computation runs in the CUDA
+kernels behind it.  Importing this module fails loudly when the library has
+not been built: there is no fallback.
+
+``matmul`` is a convenience for torch tensors: it reads shapes, dtypes, device
+pointers and the current stream, allocates C with torch and calls hgemm_run.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libhgemm.so")
+HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "hgemm.h")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        "libhgemm.so is not built (expected at %s). Build it with `python -m tensor_core_half_gb300.build` "
+        "or `python -c 'import __graft_entry__ as g; g.build()'`." % LIB_PATH)
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+# ---------------------------------------------------------------- enums ----
+HGEMM_OK = 0
+HGEMM_ERR_INVALID_ARG = 1
+HGEMM_ERR_UNSUPPORTED = 2
+HGEMM_ERR_MISALIGNED = 3
+HGEMM_ERR_ALIAS = 4
+HGEMM_ERR_NO_DEVICE = 5
+HGEMM_ERR_CUDA = 6
+HGEMM_ERR_TIMEOUT = 7
+HGEMM_ERR_OOM = 8
+
+HGEMM_LAYOUT_TN = 0
+HGEMM_LAYOUT_NN = 1
+
+HGEMM_F16 = 0
+HGEMM_BF16 = 1
+HGEMM_F32 = 2
+
+HGEMM_VARIANT_AUTO = 0
+HGEMM_VARIANT_1SM_128x128 = 1
+HGEMM_VARIANT_1SM_128x256 = 2
+HGEMM_VARIANT_2SM_256x256 = 3
+HGEMM_VARIANT_SPLITK = 4
+
+HGEMM_OPT_FORCE_VARIANT = 1
+HGEMM_OPT_TIMEOUT_NS = 2
+HGEMM_OPT_INJECT_FAULT = 3
+HGEMM_OPT_GROUP_M = 4
+HGEMM_OPT_MAX_CTAS = 5
+
+LAYOUTS = {"TN": HGEMM_LAYOUT_TN, "NN": HGEMM_LAYOUT_NN}
+DTYPES = {"f16": HGEMM_F16, "bf16": HGEMM_BF16, "f32": HGEMM_F32}
+VARIANTS = {"auto": HGEMM_VARIANT_AUTO, "1sm128": HGEMM_VARIANT_1SM_128x128, "1sm256": HGEMM_VARIANT_1SM_128x256,
+            "2sm256": HGEMM_VARIANT_2SM_256x256, "splitk": HGEMM_VARIANT_SPLITK}
+
+
+class hgemm_plan_t(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "variant", "cta_group", "tile_m", "tile_n", "block_k", "stages", "tiles_m", "tiles_n", "num_tiles",
+        "k_blocks", "grid", "group_m", "smem_bytes", "tmem_cols")] + [("workspace_bytes", ctypes.c_int64)]
+
+    def as_dict(self):
+        return {n: getattr(self, n) for n, _ in self._fields_}
+
+
+_vp = ctypes.c_void_p
+_i32 = ctypes.c_int32
+_i64 = ctypes.c_int64
+_u32 = ctypes.c_uint32
+_u64 = ctypes.c_uint64
+
+_lib.hgemm_create.restype = _i32
+_lib.hgemm_create.argtypes = [ctypes.POINTER(_vp)]
+_lib.hgemm_destroy.restype = _i32
+_lib.hgemm_destroy.argtypes = [_vp]
+_lib.hgemm_run.restype = _i32
+_lib.hgemm_run.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _i32, _i32, _i32, _vp]
+_lib.hgemm_sync_status.restype = _i32
+_lib.hgemm_sync_status.argtypes = [_vp, _vp, ctypes.POINTER(_i32)]
+_lib.hgemm_set_option.restype = _i32
+_lib.hgemm_set_option.argtypes = [_vp, _i32, _i64]
+_lib.hgemm_status_string.restype = ctypes.c_char_p
+_lib.hgemm_status_string.argtypes = [_i32]
+_lib.hgemm_plan.restype = _i32
+_lib.hgemm_plan.argtypes = [_i64, _i64, _i64, _i32, _i32, _i32, _i32, _i32, _i32, _i32, ctypes.POINTER(hgemm_plan_t)]
+_lib.hgemm_plan_tile.restype = _i32
+_lib.hgemm_plan_tile.argtypes = [ctypes.POINTER(hgemm_plan_t), _i32, ctypes.POINTER(_i32), ctypes.POINTER(_i32)]
+_lib.hgemm_plan_splitk_range.restype = _i32
+_lib.hgemm_plan_splitk_range.argtypes = [ctypes.POINTER(hgemm_plan_t), _i32, ctypes.POINTER(_i64),
+                                         ctypes.POINTER(_i64)]
+_lib.hgemm_encode_idesc.restype = _u32
+_lib.hgemm_encode_idesc.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32]
+_lib.hgemm_encode_smem_desc.restype = _u64
+_lib.hgemm_encode_smem_desc.argtypes = [_u32, _u32, _u32, _i32]
+_lib.hgemm_version.restype = _i32
+_lib.hgemm_version.argtypes = []
+
+
+class HgemmError(RuntimeError):
+    def __init__(self, status, where=""):
+        self.status = int(status)
+        super().__init__("%s%s" % (where + ": " if where else "", hgemm_status_string(status)))
+
+
+def lib():
+    """The loaded ctypes library (for symbol checks)."""
+    return _lib
+
+
+def declared_functions():
+    """Names of the functions declared in include/hgemm.h."""
+    with open(HEADER_PATH) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(hgemm_[a-z_0-9]+)\s*\(", text,
+                                 flags=re.M)))
+
+
+# ------------------------------------------------------- entry points ----
+def hgemm_status_string(status) -> str:
+    return _lib.hgemm_status_string(int(status)).decode()
+
+
+def hgemm_version() -> int:
+    return int(_lib.hgemm_version())
+
+
+def hgemm_create() -> int:
+    h = _vp()
+    st = _lib.hgemm_create(ctypes.byref(h))
+    if st != HGEMM_OK:
+        raise HgemmError(st, "hgemm_create")
+    return h.value
+
+
+def hgemm_destroy(h) -> int:
+    return int(_lib.hgemm_destroy(h))
+
+
+def hgemm_run(h, A, B, C, M, N, K, layout, in_dtype, acc_dtype, out_dtype, stream=0) -> int:
+    return int(_lib.hgemm_run(h, A, B, C, int(M), int(N), int(K), int(layout), int(in_dtype), int(acc_dtype),
+                              int(out_dtype), stream))
+
+
+def hgemm_sync_status(h, stream=0):
+    d = _i32(0)
+    st = _lib.hgemm_sync_status(h, stream, ctypes.byref(d))
+    return int(st), int(d.value)
+
+
+def hgemm_set_option(h, option, value) -> int:
+    return int(_lib.hgemm_set_option(h, int(option), int(value)))
+
+
+def hgemm_plan(M, N, K, layout=HGEMM_LAYOUT_TN, in_dtype=HGEMM_BF16, acc_dtype=HGEMM_F32, out_dtype=HGEMM_BF16,
+               num_sms=152, variant=HGEMM_VARIANT_AUTO, group_m=0):
+    p = hgemm_plan_t()
+    st = _lib.hgemm_plan(int(M), int(N), int(K), int(layout), int(in_dtype), int(acc_dtype), int(out_dtype),
+                         int(num_sms), int(variant), int(group_m), ctypes.byref(p))
+    return int(st), p
+
+
+def hgemm_plan_tile(plan, t):
+    m, n = _i32(), _i32()
+    st = _lib.hgemm_plan_tile(ctypes.byref(plan), int(t), ctypes.byref(m), ctypes.byref(n))
+    return int(st), m.value, n.value
+
+
+def hgemm_plan_splitk_range(plan, cta):
+    b, e = _i64(), _i64()
+    st = _lib.hgemm_plan_splitk_range(ctypes.byref(plan), int(cta), ctypes.byref(b), ctypes.byref(e))
+    return int(st), b.value, e.value
+
+
+def hgemm_encode_idesc(mma_m, mma_n, in_dtype, acc_dtype, a_mn_major=0, b_mn_major=0) -> int:
+    return int(_lib.hgemm_encode_idesc(int(mma_m), int(mma_n), int(in_dtype), int(acc_dtype), int(a_mn_major),
+                                       int(b_mn_major)))
+
+
+def hgemm_encode_smem_desc(addr, lbo, sbo, swizzle) -> int:
+    return int(_lib.hgemm_encode_smem_desc(int(addr), int(lbo), int(sbo), int(swizzle)))
+
+
+# ------------------------------------------------------ torch helpers ----
+_local = threading.local()
+
+
+def _default_handle():
+    h = getattr(_local, "handle", None)
+    if h is None:
+        h = Handle()
+        _local.handle = h
+    return h
+
+
+class Handle:
+    """Owns an hgemm handle bound to the current CUDA device."""
+
+    def __init__(self):
+        self.h = hgemm_create()
+
+    def close(self):
+        if self.h:
+            hgemm_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def set_option(self, option, value):
+        st = hgemm_set_option(self.h, option, value)
+        if st != HGEMM_OK:
+            raise HgemmError(st, "hgemm_set_option")
+
+    def sync_status(self, stream=None):
+        import torch
+        s = stream if stream is not None else torch.cuda.current_stream()
+        return hgemm_sync_status(self.h, s.cuda_stream)
+
+    def run(self, A, B, C, layout="TN", acc="f32", stream=None, check=True):
+        """C = A . B on torch CUDA tensors (A [M,K]; B [N,K] for TN or [K,N] for NN; C [M,N])."""
+        import torch
+        M, K = A.shape
+        N = B.shape[0] if layout == "TN" else B.shape[1]
+        s = stream if stream is not None else torch.cuda.current_stream()
+        st = hgemm_run(self.h, A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, LAYOUTS[layout],
+                       _torch_dtype(A.dtype), DTYPES[acc], _torch_dtype(C.dtype), s.cuda_stream)
+        if check and st != HGEMM_OK:
+            raise HgemmError(st, "hgemm_run")
+        return st
+
+
+def _torch_dtype(dt):
+    import torch
+    if dt == torch.float16:
+        return HGEMM_F16
+    if dt == torch.bfloat16:
+        return HGEMM_BF16
+    if dt == torch.float32:
+        return HGEMM_F32
+    raise TypeError("unsupported dtype %s" % dt)
+
+
+def matmul(A, B, layout="TN", acc="f32", out_dtype=None, out=None, handle=None, stream=None):
+    """Returns C = A . B (torch CUDA tensors, contiguous).  See Handle.run."""
+    import torch
+    if not (A.is_cuda and B.is_cuda):
+        raise ValueError("matmul needs CUDA tensors; there is no CPU path")
+    if not (A.is_contiguous() and B.is_contiguous()):
+        raise ValueError("A and B must be contiguous")
+    M = A.shape[0]
+    N = B.shape[0] if layout == "TN" else B.shape[1]
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype or A.dtype, device=A.device)
+    (handle or _default_handle()).run(A, B, out, layout=layout, acc=acc, stream=stream)
+    return out

@@ -1,0 +1,233 @@
+"""GPU parity of the CUDA path (through the C ABI) against the CPU oracle.
+
+Sizes here finish in seconds on the oracle and still span several tiles and
+ragged tails; the full workload table is covered in test_gpu_workloads.py.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests import parity
+from tensor_core_half_gb300 import hgemm, workloads
+
+pytestmark = pytest.mark.gpu
+
+TORCH_DT = {"f16": torch.float16, "bf16": torch.bfloat16}
+DENSE_VARIANTS = ["1sm128", "1sm256", "2sm256"]
+
+
+@pytest.fixture(scope="module")
+def h():
+    handle = hgemm.Handle()
+    yield handle
+    handle.close()
+
+
+def run(h, a, b, M, N, K, layout, acc, out, variant="auto", C=None):
+    h.set_option(hgemm.HGEMM_OPT_FORCE_VARIANT, hgemm.VARIANTS[variant])
+    try:
+        A, B = a.cuda(), b.cuda()
+        if C is None:
+            C = torch.empty((M, N), dtype=TORCH_DT[out], device="cuda")
+        h.run(A, B, C, layout=layout, acc=acc)
+        st, detail = h.sync_status()
+        assert st == hgemm.HGEMM_OK, (hgemm.hgemm_status_string(st), hex(detail))
+        return workloads.bits(C.cpu())
+    finally:
+        h.set_option(hgemm.HGEMM_OPT_FORCE_VARIANT, hgemm.HGEMM_VARIANT_AUTO)
+
+
+@pytest.mark.parametrize("variant", ["auto"] + DENSE_VARIANTS)
+def test_square256_f16(h, variant):
+    w = workloads.WORKLOADS["square256_f16"]
+    a, b, ab, bb = parity.inputs(w.M, w.N, w.K, w.layout, w.in_dtype, w.dist, w.seed)
+    got = run(h, a, b, w.M, w.N, w.K, w.layout, w.acc_dtype, w.out_dtype, variant)
+    parity.check(got, ab, bb, w.M, w.N, w.K, w.layout, w.in_dtype, w.acc_dtype, w.out_dtype)
+
+
+DTYPE_COMBOS = [("f16", "f32", "f16"), ("f16", "f32", "bf16"), ("bf16", "f32", "bf16"), ("bf16", "f32", "f16"),
+                ("f16", "f16", "f16"), ("f16", "f16", "bf16")]
+
+
+@pytest.mark.parametrize("variant", DENSE_VARIANTS)
+@pytest.mark.parametrize("layout", ["TN", "NN"])
+@pytest.mark.parametrize("combo", DTYPE_COMBOS, ids=["-".join(c) for c in DTYPE_COMBOS])
+def test_dtype_layout_variant_matrix(h, combo, layout, variant):
+    fin, acc, out = combo
+    M, N, K = 384, 520, 200  # ragged in M (for 256-row tiles), N and K
+    a, b, ab, bb = parity.inputs(M, N, K, layout, fin, ("uniform", -1.0, 1.0), 11)
+    got = run(h, a, b, M, N, K, layout, acc, out, variant)
+    parity.check(got, ab, bb, M, N, K, layout, fin, acc, out)
+
+
+RAGGED_M = [1, 8, 120, 128, 129, 257, 1000]
+RAGGED_N = [8, 120, 136, 264, 1000]
+
+
+@pytest.mark.parametrize("layout", ["TN", "NN"])
+@pytest.mark.parametrize("K", [8, 72, 640])
+@pytest.mark.parametrize("N", RAGGED_N)
+@pytest.mark.parametrize("M", RAGGED_M)
+def test_ragged_sweep(h, M, N, K, layout):
+    a, b, ab, bb = parity.inputs(M, N, K, layout, "bf16", ("normal", 1.0), M * 7 + N * 3 + K)
+    got = run(h, a, b, M, N, K, layout, "f32", "bf16")
+    parity.check(got, ab, bb, M, N, K, layout, "bf16", "f32", "bf16")
+
+
+@pytest.mark.parametrize("layout", ["TN", "NN"])
+@pytest.mark.parametrize("M,N", [(129, 1000), (1000, 264), (16, 1000)])
+def test_ragged_long_k(h, M, N, layout):
+    K = 4104
+    a, b, ab, bb = parity.inputs(M, N, K, layout, "f16", ("uniform", -1.0, 1.0), 5)
+    got = run(h, a, b, M, N, K, layout, "f32", "f16")
+    parity.check(got, ab, bb, M, N, K, layout, "f16", "f32", "f16")
+
+
+@pytest.mark.parametrize("variant", ["auto"] + DENSE_VARIANTS)
+@pytest.mark.parametrize("layout", ["TN", "NN"])
+def test_small_integers_bit_exact_f32_acc(h, layout, variant):
+    # |C| <= 16 * 4096 = 65536 < 2^24: every partial sum is exact in fp32, so the
+    # device result is RNE(exact) whatever the accumulation order.
+    M, N, K = 320, 384, 4096
+    a, b, ab, bb = parity.inputs(M, N, K, layout, "bf16", ("int", -4, 4), 21)
+    got = run(h, a, b, M, N, K, layout, "f32", "bf16", variant)
+    ref, _, _ = oracle.gemm(ab, bb, M, N, K, layout, "bf16", "bf16")
+    assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("variant", DENSE_VARIANTS)
+def test_small_integers_bit_exact_f16_acc(h, variant):
+    # {-1,0,1} with K <= 2048: every partial sum is an integer of magnitude <= 2048,
+    # exactly representable in fp16.
+    M, N, K = 256, 256, 2048
+    a, b, ab, bb = parity.inputs(M, N, K, "TN", "f16", ("int", -1, 1), 22)
+    got = run(h, a, b, M, N, K, "TN", "f16", "f16", variant)
+    ref, _, _ = oracle.gemm(ab, bb, M, N, K, "TN", "f16", "f16")
+    assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("M", [1, 5, 16, 17, 33, 48, 64])
+@pytest.mark.parametrize("N,K", [(8, 64), (1000, 72), (4096, 1024), (384, 8192)])
+def test_splitk_shapes(h, M, N, K):
+    a, b, ab, bb = parity.inputs(M, N, K, "TN", "bf16", ("normal", 0.02), 4)
+    got = run(h, a, b, M, N, K, "TN", "f32", "bf16", "splitk")
+    parity.check(got, ab, bb, M, N, K, "TN", "bf16", "f32", "bf16")
+
+
+def test_splitk_small_integers_bit_exact(h):
+    M, N, K = 16, 2048, 4096
+    a, b, ab, bb = parity.inputs(M, N, K, "TN", "f16", ("int", -4, 4), 23)
+    got = run(h, a, b, M, N, K, "TN", "f32", "f16", "splitk")
+    ref, _, _ = oracle.gemm(ab, bb, M, N, K, "TN", "f16", "f16")
+    assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("variant,M", [("2sm256", 640), ("1sm256", 640), ("1sm128", 640), ("splitk", 40)])
+def test_run_to_run_determinism(h, variant, M):
+    N, K = 1024, 2048
+    a, b, _, _ = parity.inputs(M, N, K, "TN", "bf16", ("normal", 1.0), 31)
+    first = run(h, a, b, M, N, K, "TN", "f32", "bf16", variant)
+    for _ in range(3):
+        assert np.array_equal(run(h, a, b, M, N, K, "TN", "f32", "bf16", variant), first)
+
+
+@pytest.mark.parametrize("layout", ["TN", "NN"])
+def test_variants_agree_bitwise(h, layout):
+    # The dense variants differ only in data movement and tile shape; each output
+    # is one tensor-core accumulation over K in the same order.
+    M, N, K = 512, 512, 1024
+    a, b, _, _ = parity.inputs(M, N, K, layout, "f16", ("uniform", -1.0, 1.0), 32)
+    outs = [run(h, a, b, M, N, K, layout, "f32", "f16", v) for v in DENSE_VARIANTS]
+    for o in outs[1:]:
+        assert np.array_equal(o, outs[0])
+
+
+@pytest.mark.parametrize("variant,M,N,K", [("2sm256", 300, 264, 200), ("1sm128", 130, 136, 72),
+                                           ("splitk", 17, 520, 200), ("1sm256", 1, 8, 8)])
+def test_guard_bands_untouched(h, variant, M, N, K):
+    a, b, ab, bb = parity.inputs(M, N, K, "TN", "bf16", ("normal", 1.0), 41)
+    pad = 4096
+    buf = torch.full((pad + M * N + pad,), 0x7E7E, dtype=torch.int16, device="cuda")
+    C = buf[pad:pad + M * N].view(torch.bfloat16).view(M, N)
+    got = run(h, a, b, M, N, K, "TN", "f32", "bf16", variant, C=C)
+    parity.check(got, ab, bb, M, N, K, "TN", "bf16", "f32", "bf16")
+    host = buf.cpu().numpy()
+    assert np.all(host[:pad] == 0x7E7E) and np.all(host[pad + M * N:] == 0x7E7E)
+
+
+def test_k_zero_fills_zero(h):
+    M, N = 100, 72
+    C = torch.full((M, N), 3.0, dtype=torch.float16, device="cuda")
+    A = torch.empty((M, 0), dtype=torch.float16, device="cuda")
+    B = torch.empty((N, 0), dtype=torch.float16, device="cuda")
+    st = hgemm.hgemm_run(h.h, A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, 0, hgemm.HGEMM_LAYOUT_TN,
+                         hgemm.HGEMM_F16, hgemm.HGEMM_F32, hgemm.HGEMM_F16, torch.cuda.current_stream().cuda_stream)
+    assert st == hgemm.HGEMM_OK
+    assert h.sync_status()[0] == hgemm.HGEMM_OK
+    bits = workloads.bits(C.cpu())
+    assert np.all(bits == 0)  # +0, not -0
+
+
+def test_empty_m_or_n_is_noop(h):
+    C = torch.full((4, 8), 1.0, dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    for M, N in [(0, 8), (4, 0)]:
+        assert hgemm.hgemm_run(h.h, 0, 0, C.data_ptr(), M, N, 64, 0, 1, 2, 1, s) == hgemm.HGEMM_OK
+    assert h.sync_status()[0] == hgemm.HGEMM_OK
+    assert torch.all(C == 1.0)
+
+
+def test_argument_validation(h):
+    s = torch.cuda.current_stream().cuda_stream
+    A = torch.zeros((64, 64), dtype=torch.float16, device="cuda")
+    B = torch.zeros((64, 64), dtype=torch.float16, device="cuda")
+    C = torch.zeros((64, 64), dtype=torch.float16, device="cuda")
+    a, b, c = A.data_ptr(), B.data_ptr(), C.data_ptr()
+    F16, BF16, F32 = hgemm.HGEMM_F16, hgemm.HGEMM_BF16, hgemm.HGEMM_F32
+    R = hgemm.hgemm_run
+    assert R(0, a, b, c, 64, 64, 64, 0, F16, F32, F16, s) == hgemm.HGEMM_ERR_INVALID_ARG
+    assert R(h.h, 0, b, c, 64, 64, 64, 0, F16, F32, F16, s) == hgemm.HGEMM_ERR_INVALID_ARG
+    assert R(h.h, a, 0, c, 64, 64, 64, 0, F16, F32, F16, s) == hgemm.HGEMM_ERR_INVALID_ARG
+    assert R(h.h, a, b, 0, 64, 64, 64, 0, F16, F32, F16, s) == hgemm.HGEMM_ERR_INVALID_ARG
+    assert R(h.h, a, b, c, -1, 64, 64, 0, F16, F32, F16, s) == hgemm.HGEMM_ERR_INVALID_ARG
+    assert R(h.h, a, b, c, 64, 64, 1 << 31, 0, F16, F32, F16, s) == hgemm.HGEMM_ERR_INVALID_ARG
+    assert R(h.h, a, b, c, 64, 64, 64, 2, F16, F32, F16, s) == hgemm.HGEMM_ERR_INVALID_ARG
+    assert R(h.h, a, b, c, 64, 64, 64, 0, 7, F32, F16, s) == hgemm.HGEMM_ERR_INVALID_ARG
+    assert R(h.h, a, b, c, 64, 64, 64, 0, BF16, F16, F16, s) == hgemm.HGEMM_ERR_UNSUPPORTED
+    assert R(h.h, a, b, c, 64, 64, 64, 0, F32, F32, F16, s) == hgemm.HGEMM_ERR_UNSUPPORTED
+    assert R(h.h, a, b, c, 64, 64, 64, 0, F16, F32, F32, s) == hgemm.HGEMM_ERR_UNSUPPORTED
+    assert R(h.h, a + 2, b, c, 64, 64, 64, 0, F16, F32, F16, s) == hgemm.HGEMM_ERR_MISALIGNED
+    assert R(h.h, a, b + 8, c, 64, 64, 56, 0, F16, F32, F16, s) == hgemm.HGEMM_ERR_MISALIGNED
+    assert R(h.h, a, b, c + 2, 64, 56, 64, 0, F16, F32, F16, s) == hgemm.HGEMM_ERR_MISALIGNED
+    assert R(h.h, a, b, c, 64, 60, 64, 0, F16, F32, F16, s) == hgemm.HGEMM_ERR_MISALIGNED   # N % 8
+    assert R(h.h, a, b, c, 64, 64, 60, 0, F16, F32, F16, s) == hgemm.HGEMM_ERR_MISALIGNED   # K % 8
+    assert R(h.h, a, b, a, 64, 64, 64, 0, F16, F32, F16, s) == hgemm.HGEMM_ERR_ALIAS
+    assert R(h.h, a, b, b + 128, 8, 8, 64, 0, F16, F32, F16, s) == hgemm.HGEMM_ERR_ALIAS
+    assert h.sync_status()[0] == hgemm.HGEMM_OK
+    assert torch.all(C == 0)  # nothing was launched
+
+
+@pytest.mark.parametrize("variant,M", [("1sm128", 512), ("2sm256", 512), ("splitk", 16)])
+def test_bounded_wait_gives_up_and_recovers(h, variant, M):
+    # The first CTA's producer drops its first stage; the MMA warp's wait on that
+    # stage can never succeed, gives up after the limit, and every role exits.
+    N, K = 1024, 1024
+    a, b, ab, bb = parity.inputs(M, N, K, "TN", "bf16", ("normal", 1.0), 51)
+    A, B = a.cuda(), b.cuda()
+    C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    h.set_option(hgemm.HGEMM_OPT_FORCE_VARIANT, hgemm.VARIANTS[variant])
+    h.set_option(hgemm.HGEMM_OPT_TIMEOUT_NS, 20_000_000)
+    h.set_option(hgemm.HGEMM_OPT_INJECT_FAULT, 1)
+    try:
+        h.run(A, B, C, layout="TN", acc="f32")
+        st, detail = h.sync_status()
+        assert st == hgemm.HGEMM_ERR_TIMEOUT, (st, hex(detail))
+        assert (detail & 0xFF) == hgemm.HGEMM_ERR_TIMEOUT and ((detail >> 8) & 0xFF) in (1, 2, 3, 4)
+    finally:
+        h.set_option(hgemm.HGEMM_OPT_INJECT_FAULT, 0)
+        h.set_option(hgemm.HGEMM_OPT_TIMEOUT_NS, 2_000_000_000)
+        h.set_option(hgemm.HGEMM_OPT_FORCE_VARIANT, hgemm.HGEMM_VARIANT_AUTO)
+    # the context is still usable and the next launch is correct
+    got = run(h, a, b, M, N, K, "TN", "f32", "bf16", variant)
+    parity.check(got, ab, bb, M, N, K, "TN", "bf16", "f32", "bf16")
