@@ -1,0 +1,162 @@
+"""Host-side tests of the C ABI (no GPU): symbols, validation, planning,
+the persistent scheduler's tile map, the split-K partition and the tcgen05
+descriptor encodings."""
+import ctypes
+
+import pytest
+import torch
+
+from tensor_core_half_gb300 import hgemm
+
+H = hgemm
+ST_OK, ST_INV, ST_UNS, ST_MIS = H.HGEMM_OK, H.HGEMM_ERR_INVALID_ARG, H.HGEMM_ERR_UNSUPPORTED, H.HGEMM_ERR_MISALIGNED
+
+
+def test_library_exports_every_declared_symbol():
+    names = H.declared_functions()
+    assert len(names) >= 12
+    lib = H.lib()
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings():
+    for s in range(0, 9):
+        assert H.hgemm_status_string(s).startswith("HGEMM_")
+    assert "unknown" in H.hgemm_status_string(99)
+    assert H.hgemm_version() >= 100
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
+def test_create_without_device_reports_no_device():
+    with pytest.raises(H.HgemmError) as e:
+        H.hgemm_create()
+    assert e.value.status == H.HGEMM_ERR_NO_DEVICE
+
+
+def test_null_handle_is_rejected():
+    assert H.hgemm_run(None, 16, 16, 16, 8, 8, 8, 0, 0, 2, 0, None) == ST_INV
+    assert H.hgemm_sync_status(None)[0] == ST_INV
+    assert H.hgemm_set_option(None, H.HGEMM_OPT_GROUP_M, 4) == ST_INV
+    assert H.hgemm_destroy(None) == ST_OK
+
+
+def plan(M, N, K, layout=0, fin=1, acc=2, out=1, sms=152, variant=0, group_m=0):
+    return H.hgemm_plan(M, N, K, layout, fin, acc, out, sms, variant, group_m)
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((-1, 8, 8), ST_INV), ((8, -1, 8), ST_INV), ((8, 8, -1), ST_INV), ((1 << 31, 8, 8), ST_INV),
+    ((8, 12, 8), ST_MIS), ((8, 8, 12), ST_MIS), ((0, 12, 8), ST_OK), ((8, 0, 8), ST_OK), ((8, 8, 0), ST_OK),
+    ((3, 8, 8), ST_OK)])
+def test_plan_size_validation(args, expect):
+    assert plan(*args)[0] == expect
+
+
+def test_plan_dtype_and_layout_validation():
+    assert plan(64, 64, 64, layout=2)[0] == ST_INV
+    assert plan(64, 64, 64, fin=5)[0] == ST_INV
+    assert plan(64, 64, 64, fin=H.HGEMM_BF16, acc=H.HGEMM_F16)[0] == ST_UNS
+    assert plan(64, 64, 64, fin=H.HGEMM_F32)[0] == ST_UNS
+    assert plan(64, 64, 64, out=H.HGEMM_F32)[0] == ST_UNS
+    assert plan(64, 64, 64, acc=H.HGEMM_BF16)[0] == ST_UNS
+    assert plan(64, 64, 64, fin=H.HGEMM_F16, acc=H.HGEMM_F16, out=H.HGEMM_F16)[0] == ST_OK
+    assert plan(64, 64, 64, sms=0)[0] == ST_INV
+    assert plan(64, 64, 64, variant=9)[0] == ST_INV
+
+
+def test_plan_variant_choice():
+    st, p = plan(4096, 4096, 4096)
+    assert st == ST_OK and p.variant == H.HGEMM_VARIANT_2SM_256x256 and p.cta_group == 2
+    assert (p.tile_m, p.tile_n, p.tiles_m, p.tiles_n, p.num_tiles, p.k_blocks) == (256, 256, 16, 16, 256, 64)
+    assert p.grid == 152 and p.tmem_cols == 512 and p.smem_bytes <= 232448
+    st, p = plan(16, 16384, 8192)
+    assert st == ST_OK and p.variant == H.HGEMM_VARIANT_SPLITK and p.tile_n == 16 and p.num_tiles == 128
+    assert p.grid == 152 and p.k_blocks == 128 and p.workspace_bytes > 0
+    st, p = plan(16, 16384, 8192, layout=H.HGEMM_LAYOUT_NN)
+    assert st == ST_OK and p.variant != H.HGEMM_VARIANT_SPLITK  # split-K is TN only
+    st, p = plan(16, 16384, 8192, fin=0, acc=0, out=0)
+    assert st == ST_OK and p.variant != H.HGEMM_VARIANT_SPLITK  # and fp32 accumulate only
+    assert plan(16, 64, 64, layout=1, variant=H.HGEMM_VARIANT_SPLITK)[0] == ST_UNS
+    assert plan(65, 64, 64, variant=H.HGEMM_VARIANT_SPLITK)[0] == ST_UNS
+    for v in (1, 2, 3):
+        st, p = plan(1000, 3000, 4104, variant=v)
+        assert st == ST_OK and p.variant == v
+    st, p = plan(1000, 3000, 4104, variant=1)
+    assert (p.tiles_m, p.tiles_n, p.k_blocks) == (8, 24, 65)
+
+
+@pytest.mark.parametrize("M,N,K,variant", [(4096, 4096, 4096, 3), (1000, 3000, 4104, 1), (1000, 3000, 4104, 2),
+                                           (8192, 8192, 64, 3), (129, 8, 8, 3), (5000, 136, 64, 1)])
+@pytest.mark.parametrize("group_m", [1, 3, 8, 100])
+def test_tile_map_is_a_bijection(M, N, K, variant, group_m):
+    st, p = plan(M, N, K, variant=variant, group_m=group_m)
+    assert st == ST_OK
+    seen = set()
+    for t in range(p.num_tiles):
+        s, m, n = H.hgemm_plan_tile(p, t)
+        assert s == ST_OK and 0 <= m < p.tiles_m and 0 <= n < p.tiles_n
+        seen.add((m, n))
+    assert len(seen) == p.num_tiles
+    assert H.hgemm_plan_tile(p, p.num_tiles)[0] == ST_INV
+    assert H.hgemm_plan_tile(p, -1)[0] == ST_INV
+
+
+def test_tile_map_groups_rows():
+    # Within a full group, consecutive tiles walk down group_m tile rows before
+    # moving one tile column right ("block swizzle" band order).
+    st, p = plan(4096, 4096, 4096, variant=3, group_m=4)
+    coords = [H.hgemm_plan_tile(p, t)[1:] for t in range(12)]
+    assert coords[:5] == [(0, 0), (1, 0), (2, 0), (3, 0), (0, 1)]
+    assert coords[8] == (0, 2)
+    # the last group is shorter when tiles_m is not a multiple of group_m
+    st, p = plan(5 * 256, 512, 64, variant=3, group_m=4)
+    tail = [H.hgemm_plan_tile(p, t)[1:] for t in range(8, 10)]
+    assert tail == [(4, 0), (4, 1)]
+
+
+@pytest.mark.parametrize("M,N,K,sms", [(16, 16384, 8192, 152), (1, 8, 64, 152), (64, 1000, 72, 152),
+                                       (16, 4096, 4096, 7), (33, 100000, 640, 152), (16, 128, 8192, 152)])
+def test_splitk_partition(M, N, K, sms):
+    st, p = plan(M, N, K, sms=sms)
+    assert st == ST_OK and p.variant == H.HGEMM_VARIANT_SPLITK
+    units = p.num_tiles * p.k_blocks
+    prev_end, sizes = 0, []
+    for c in range(p.grid):
+        s, b, e = H.hgemm_plan_splitk_range(p, c)
+        assert s == ST_OK and b == prev_end and e > b
+        sizes.append(e - b)
+        prev_end = e
+    assert prev_end == units
+    assert max(sizes) - min(sizes) <= 1
+    assert H.hgemm_plan_splitk_range(p, p.grid)[0] == ST_INV
+
+
+# ------------------------------------------------------------ descriptors ----
+# Expected words are written out by hand from the field tables:
+#   idesc: D fmt bits 4-5 (f32 = 1), A fmt 7-9 / B fmt 10-12 (bf16 = 1),
+#          A major bit 15, B major bit 16, N>>3 at 17-22, M>>4 at 24-28.
+#   smem desc: addr>>4 at 0-13, LBO>>4 at 16-29, SBO>>4 at 32-45, bit 46 = 1,
+#          swizzle at 61-63 (128-byte swizzle = 2).
+@pytest.mark.parametrize("args,word", [
+    ((128, 256, H.HGEMM_BF16, H.HGEMM_F32, 0, 0), 0x08400490),  # 0x10|0x80|0x400|(32<<17)|(8<<24)
+    ((256, 256, H.HGEMM_BF16, H.HGEMM_F32, 0, 0), 0x10400490),  # M=256: 16<<24
+    ((128, 128, H.HGEMM_F16, H.HGEMM_F32, 0, 0), 0x08200010),   # fp16 in: format 0; N=128: 16<<17
+    ((128, 128, H.HGEMM_F16, H.HGEMM_F16, 0, 0), 0x08200000),   # fp16 accumulate: D format 0
+    ((128, 16, H.HGEMM_BF16, H.HGEMM_F32, 0, 0), 0x08040490),   # N=16: 2<<17
+    ((256, 256, H.HGEMM_F16, H.HGEMM_F32, 0, 1), 0x10410010),   # NN: B MN-major bit 16
+    ((128, 64, H.HGEMM_F16, H.HGEMM_F32, 1, 0), 0x08108010),    # A MN-major bit 15; N=64: 8<<17
+])
+def test_instruction_descriptor_bits(args, word):
+    assert H.hgemm_encode_idesc(*args) == word
+
+
+@pytest.mark.parametrize("args,word", [
+    ((0x400, 16, 1024, 2), 0x4000404000010040),
+    ((0x1C400 + 32, 16, 1024, 2), 0x4000404000011C42),   # +32 B K step inside the swizzle atom
+    ((0x2000, 8192, 1024, 2), 0x4000404002000200),       # MN-major: LBO 8 KiB
+    ((0x0, 128, 1024, 0), 0x0000404000080000),           # no swizzle
+    ((0x3FFF0, 0, 0, 2), 0x4000400000003FFF),            # top of the 18-bit shared window
+])
+def test_shared_memory_descriptor_bits(args, word):
+    assert H.hgemm_encode_smem_desc(*args) == word
