@@ -190,6 +190,41 @@ uint32_t hgemm_encode_idesc(int32_t mma_m, int32_t mma_n, hgemm_dtype_t in_dtype
  */
 uint64_t hgemm_encode_smem_desc(uint32_t smem_addr, uint32_t lbo_bytes, uint32_t sbo_bytes, int32_t swizzle_mode);
 
+/*
+ * hgemm_run_splitk_noalloc -- C = A . B for skinny M without allocating any
+ * device memory and without a handle.
+ *
+ * The pages have no counterpart for this entry point.  It exists for callers
+ * that cannot call cudaMalloc while they multiply (code inside a caching
+ * allocator or an out-of-memory handler, a process whose device memory is
+ * all held by its own pool, latency-critical loops that cannot take
+ * cudaMalloc's implicit synchronisation): such callers can neither create a
+ * handle nor let hgemm_run grow its split-K workspace.
+ *
+ * It runs the split-K kernel of hgemm_run (TN layout, fp32 accumulation) with
+ * its scratch -- partial sums, per-tile tickets and a status word -- in a
+ * fixed 16 MiB array inside the library's device image, which every GPU that
+ * loads the library holds until the process exits.  No cudaMalloc, cudaFree
+ * or allocating library routine is called.
+ *   A: device pointer, M x K row-major; B: device pointer, N x K row-major
+ *   (TN); C: device pointer, M x N row-major, written.  The caller owns all three.
+ *   Limits: 1 <= M <= 64 and N <= 33,554,432 (ceil(N/128) tickets fit in
+ *   1 MiB); larger sizes return HGEMM_ERR_UNSUPPORTED.  M == 0 or N == 0 is a
+ *   no-op; K == 0 writes +0.  Alignment and aliasing rules are those of
+ *   hgemm_run (HGEMM_ERR_MISALIGNED, HGEMM_ERR_ALIAS, HGEMM_ERR_INVALID_ARG).
+ *   in_dtype, out_dtype: HGEMM_F16 or HGEMM_BF16.
+ * The first call on each device does a one-time set-up with that device
+ * current (the array's device address, the SM count, the kernel's shared-
+ * memory limit); make that first call before any stream capture.  Every call
+ * clears the status word and the tickets it uses, on `stream`, before the
+ * kernel.  All calls on a device share the one array, so calls whose kernels
+ * overlap on the GPU (different streams without ordering) race and give
+ * wrong results.  A device-side wait that gives up is not reported: there is
+ * no handle to read a status from.
+ */
+hgemm_status_t hgemm_run_splitk_noalloc(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                                        hgemm_dtype_t in_dtype, hgemm_dtype_t out_dtype, void* stream);
+
 /* Library version, e.g. 100 for 0.1.0. */
 int32_t hgemm_version(void);
 

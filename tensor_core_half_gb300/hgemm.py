@@ -102,6 +102,8 @@ _lib.hgemm_encode_smem_desc.restype = _u64
 _lib.hgemm_encode_smem_desc.argtypes = [_u32, _u32, _u32, _i32]
 _lib.hgemm_version.restype = _i32
 _lib.hgemm_version.argtypes = []
+_lib.hgemm_run_splitk_noalloc.restype = _i32
+_lib.hgemm_run_splitk_noalloc.argtypes = [_vp, _vp, _vp, _i64, _i64, _i64, _i32, _i32, _vp]
 
 
 class HgemmError(RuntimeError):
@@ -187,6 +189,12 @@ def hgemm_encode_idesc(mma_m, mma_n, in_dtype, acc_dtype, a_mn_major=0, b_mn_maj
 
 def hgemm_encode_smem_desc(addr, lbo, sbo, swizzle) -> int:
     return int(_lib.hgemm_encode_smem_desc(int(addr), int(lbo), int(sbo), int(swizzle)))
+
+
+def hgemm_run_splitk_noalloc(A, B, C, M, N, K, in_dtype, out_dtype, stream=0) -> int:
+    """Skinny-M product with scratch in a fixed device array: no allocation,
+    no handle (for callers that cannot allocate device memory)."""
+    return int(_lib.hgemm_run_splitk_noalloc(A, B, C, int(M), int(N), int(K), int(in_dtype), int(out_dtype), stream))
 
 
 # ------------------------------------------------------ torch helpers ----
