@@ -69,8 +69,27 @@ typedef enum {
   HGEMM_OPT_INJECT_FAULT = 3,  /* value: 0 off; 1 = the first CTA's producer drops its first
                                   stage, so the consumer's bounded wait must give up (tests)  */
   HGEMM_OPT_GROUP_M = 4,       /* value: rasterisation group height in tiles (default 8)      */
-  HGEMM_OPT_MAX_CTAS = 5       /* value: cap on persistent CTAs (0 = one per SM)              */
+  HGEMM_OPT_MAX_CTAS = 5,      /* value: cap on persistent CTAs (0 = one per SM)              */
+  HGEMM_OPT_STREAM_K = 6,      /* value: 1 (default) lets the planner split the last wave of
+                                  dense tiles along K (stream-K); 0 keeps every tile whole    */
+  HGEMM_OPT_TRACE = 7          /* value: capacity in events of a device trace buffer that the
+                                  kernels append to (0 = off, the default); hgemm_trace_read */
 } hgemm_option_t;
+
+/* One intra-kernel trace event (HGEMM_OPT_TRACE).  t_ns is the GPU's global
+ * nanosecond timer.  role: 0 CTA, 1 TMA producer, 2 MMA issuer, 3 epilogue.
+ * kind: 1 kernel begin, 2 kernel end (after setup / before teardown), 3 item
+ * begin, 4 item end, 5 stream-K partial stored (value = ticket drawn), 6 split
+ * tile reduced (value = contributors).  item = tile index (-1 if none); value
+ * for item begin/end = first / last k-block (epilogue: the stream-K slot). */
+typedef struct {
+  uint64_t t_ns;
+  uint32_t cta;
+  uint16_t role;
+  uint16_t kind;
+  int32_t item;
+  int32_t value;
+} hgemm_trace_record_t;
 
 /*
  * hgemm_create -- bind a new handle to the CURRENT CUDA device.
@@ -122,8 +141,18 @@ hgemm_status_t hgemm_run(hgemm_handle_t h, const void* A, const void* B, void* C
  */
 hgemm_status_t hgemm_sync_status(hgemm_handle_t h, void* stream, int32_t* detail);
 
-/* Set a handle option (hgemm_option_t).  INVALID_ARG for an unknown option or value. */
+/* Set a handle option (hgemm_option_t).  INVALID_ARG for an unknown option or
+ * value; OOM when the trace buffer cannot be allocated. */
 hgemm_status_t hgemm_set_option(hgemm_handle_t h, int32_t option, int64_t value);
+
+/*
+ * hgemm_trace_read -- synchronise the device, copy up to `capacity` recorded
+ * events (oldest first in append order, which is not time order) to `out`
+ * (host memory, capacity records), store in *n_events how many were recorded
+ * since the last read (may exceed both capacities: the excess was dropped),
+ * and empty the buffer.  INVALID_ARG when tracing is off.
+ */
+hgemm_status_t hgemm_trace_read(hgemm_handle_t h, hgemm_trace_record_t* out, int64_t capacity, int64_t* n_events);
 
 /* Static, human-readable name of a status code. */
 const char* hgemm_status_string(hgemm_status_t s);
@@ -146,18 +175,32 @@ typedef struct {
   int32_t group_m;       /* rasterisation group height (tiles)                           */
   int32_t smem_bytes;    /* dynamic shared memory per CTA                                */
   int32_t tmem_cols;     /* tensor-memory columns allocated per CTA                      */
-  int64_t workspace_bytes; /* split-K partial sums + tickets                             */
+  int64_t workspace_bytes; /* split-K / stream-K partial sums + tickets                  */
+  int32_t dp_tiles;      /* dense: tiles computed whole, dealt round-robin (all if no stream-K) */
+  int32_t stream_k;      /* dense: 1 when the remaining tiles are split along K            */
+  int64_t sk_units;      /* dense: (num_tiles - dp_tiles) * k_blocks, cut evenly over clusters */
 } hgemm_plan_t;
 
 /*
  * hgemm_plan -- the launch plan hgemm_run would use for these arguments on a
  * GPU with `num_sms` SMs (cluster capacity assumed num_sms / 2 pairs).
- * `variant` = HGEMM_VARIANT_AUTO or a forced variant.  Validates the sizes,
- * dtypes and layout like hgemm_run (pointers are not involved).
+ * `variant` = HGEMM_VARIANT_AUTO or a forced variant; group_m = 0 for the
+ * default; stream_k = 1 to allow stream-K, 0 to forbid it.  Validates the
+ * sizes, dtypes and layout like hgemm_run (pointers are not involved).
  */
 hgemm_status_t hgemm_plan(int64_t M, int64_t N, int64_t K, hgemm_layout_t layout, hgemm_dtype_t in_dtype,
                           hgemm_dtype_t acc_dtype, hgemm_dtype_t out_dtype, int32_t num_sms, int32_t variant,
-                          int32_t group_m, hgemm_plan_t* plan);
+                          int32_t group_m, int32_t stream_k, hgemm_plan_t* plan);
+
+/*
+ * hgemm_plan_work_item -- the index-th item of cluster `cluster`'s work list
+ * in a dense plan: k-blocks [*kb0, *kb1) of linear tile *tile; *slot = -1 for
+ * a whole tile, 0 or 1 for a stream-K partial (first or last item of the
+ * cluster's stream-K range).  INVALID_ARG past the end of the list.  The same
+ * iterator runs on the device in the producer, MMA and epilogue roles.
+ */
+hgemm_status_t hgemm_plan_work_item(const hgemm_plan_t* plan, int32_t cluster, int32_t index, int32_t* tile,
+                                    int32_t* kb0, int32_t* kb1, int32_t* slot);
 
 /*
  * hgemm_plan_tile -- the persistent scheduler's map from a linear tile index

@@ -13,6 +13,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <algorithm>
 #include <mutex>
 #include <new>
 
@@ -45,6 +46,9 @@ struct Ctx {
   int inject = 0;
   int group_m = kDefaultGroupM;
   int max_ctas = 0;
+  bool stream_k = true;
+  TraceBuf* trace = nullptr;  // device trace buffer (HGEMM_OPT_TRACE)
+  int64_t trace_capacity = 0;
   int capacity[3] = {0, 0, 0};  // resident clusters per dense kind
   int splitk_prepared_smem = 0;
 };
@@ -94,7 +98,43 @@ int variant_of(DenseKind k) {
   }
 }
 
-void fill_dense_plan(DenseKind kind, int64_t M, int64_t N, int64_t K, int capacity, int group_m, int max_ctas,
+// A dense schedule: data-parallel tiles, then an optional stream-K range.
+struct DenseChoice {
+  double cost;        // estimated time in units of one full tile on one CTA pair
+  int clusters;       // persistent clusters launched
+  int dp_tiles;       // tiles computed whole
+  int64_t sk_units;   // k-block units of the stream-K range
+};
+
+// Data-parallel: ceil(T / P) rounds of whole tiles.  Stream-K: the last round
+// plus the remainder (T mod P tiles) is cut into equal k-block ranges, so the
+// time is T / P tiles plus the fix-up of the split tiles, which costs about 30
+// k-blocks of mainloop time per cluster (measured on GB300 with the kernel's
+// event trace: publishing or reducing a 256 x 256 fp32 partial).
+DenseChoice dense_choice(DenseKind kind, int64_t M, int64_t N, int64_t K, int capacity, int max_ctas,
+                         bool allow_sk) {
+  const DenseKindInfo info = dense_kind_info(kind);
+  const int64_t tiles = cdiv(M, 128 * info.cta_group) * cdiv(N, info.block_n);
+  const int64_t kb = cdiv(K, 64);
+  int64_t P = capacity > 0 ? capacity : 1;
+  if (max_ctas > 0) P = std::max<int64_t>(1, std::min<int64_t>(P, max_ctas / info.cta_group));
+  DenseChoice dp{(double)cdiv(tiles, P), (int)std::min<int64_t>(tiles, P), (int)tiles, 0};
+  DenseChoice best = dp;
+  if (allow_sk && kb >= 2 && tiles % P != 0) {
+    const int64_t waves = tiles / P;
+    DenseChoice sk;
+    sk.dp_tiles = (int)(waves >= 1 ? (waves - 1) * P : 0);
+    sk.sk_units = (tiles - sk.dp_tiles) * kb;
+    sk.clusters = (int)std::min<int64_t>(P, sk.sk_units);
+    sk.cost = (double)tiles / (double)sk.clusters + 30.0 / (double)kb;
+    if (sk.cost < dp.cost) best = sk;
+  }
+  const double eff = (kind == kDense2Sm256) ? 1.0 : (kind == kDense1Sm256 ? 0.85 : 0.70);
+  best.cost *= (double)(128 * info.cta_group) * (double)info.block_n / (double)info.cta_group / eff;
+  return best;
+}
+
+void fill_dense_plan(DenseKind kind, const DenseChoice& ch, int64_t M, int64_t N, int64_t K, int group_m,
                      hgemm_plan_t* p) {
   const DenseKindInfo info = dense_kind_info(kind);
   p->variant = variant_of(kind);
@@ -107,35 +147,22 @@ void fill_dense_plan(DenseKind kind, int64_t M, int64_t N, int64_t K, int capaci
   p->tiles_n = (int32_t)cdiv(N, p->tile_n);
   p->num_tiles = p->tiles_m * p->tiles_n;
   p->k_blocks = (int32_t)cdiv(K, 64);
-  int clusters = capacity > 0 ? capacity : 1;
-  if (max_ctas > 0) {
-    int cap = max_ctas / info.cta_group;
-    if (cap < 1) cap = 1;
-    if (cap < clusters) clusters = cap;
-  }
-  if (p->num_tiles < clusters) clusters = p->num_tiles;
-  p->grid = clusters * info.cta_group;
+  p->grid = ch.clusters * info.cta_group;
   p->group_m = group_m > 0 ? group_m : kDefaultGroupM;
   p->smem_bytes = info.smem_bytes;
   p->tmem_cols = info.tmem_cols;
-  p->workspace_bytes = 0;
-}
-
-// Estimated relative cost of a dense plan: waves of tiles x tile work / efficiency.
-double dense_cost(DenseKind kind, int64_t M, int64_t N, int capacity) {
-  const DenseKindInfo info = dense_kind_info(kind);
-  const int64_t tm = 128 * info.cta_group, tn = info.block_n;
-  const int64_t tiles = cdiv(M, tm) * cdiv(N, tn);
-  const int64_t slots = capacity > 0 ? capacity : 1;
-  const int64_t waves = cdiv(tiles, slots);
-  const double eff = (kind == kDense2Sm256) ? 1.0 : (kind == kDense1Sm256 ? 0.85 : 0.70);
-  // one wave of the whole chip does `slots` tiles, each (tm x tn) / per-SM share
-  return (double)waves * (double)(tm * tn) / (double)info.cta_group / eff;
+  p->dp_tiles = ch.dp_tiles;
+  p->sk_units = ch.sk_units;
+  p->stream_k = ch.sk_units > 0 ? 1 : 0;
+  p->workspace_bytes =
+      p->stream_k ? (int64_t)ch.clusters * 2 * info.cta_group * info.block_n * 128 * 4 +
+                        (int64_t)p->num_tiles * info.cta_group * 8
+                  : 0;
 }
 
 hgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int layout, int in, int acc, int out, int num_sms,
                          int smem_optin, const int capacity_in[3], int variant, int group_m, int max_ctas,
-                         hgemm_plan_t* p) {
+                         bool allow_sk, hgemm_plan_t* p) {
   memset(p, 0, sizeof(*p));
   hgemm_status_t st = check_problem(M, N, K, layout, in, acc, out);
   if (st != HGEMM_OK) return st;
@@ -176,21 +203,23 @@ hgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int layout, int in, in
     p->workspace_bytes = (int64_t)splitk_workspace_bytes(p->grid, mma_n, p->num_tiles);
     return HGEMM_OK;
   }
-  DenseKind kind;
+  DenseKind kind = kDense2Sm256;
+  DenseChoice choice{};
   if (variant != HGEMM_VARIANT_AUTO) {
     kind = kind_of(variant);
+    choice = dense_choice(kind, M, N, K, capacity[kind], max_ctas, allow_sk);
   } else {
-    kind = kDense2Sm256;
-    double best = dense_cost(kDense2Sm256, M, N, capacity[kDense2Sm256]);
-    for (DenseKind k : {kDense1Sm256, kDense1Sm128}) {
-      const double c = dense_cost(k, M, N, capacity[k]);
-      if (c < best) {
-        best = c;
+    bool first = true;
+    for (DenseKind k : {kDense2Sm256, kDense1Sm256, kDense1Sm128}) {
+      const DenseChoice c = dense_choice(k, M, N, K, capacity[k], max_ctas, allow_sk);
+      if (first || c.cost < choice.cost) {
+        choice = c;
         kind = k;
+        first = false;
       }
     }
   }
-  fill_dense_plan(kind, M, N, K, capacity[kind], group_m, max_ctas, p);
+  fill_dense_plan(kind, choice, M, N, K, group_m, p);
   return HGEMM_OK;
 }
 
@@ -217,7 +246,8 @@ hgemm_status_t cuda_status(cudaError_t e) {
   return HGEMM_ERR_CUDA;
 }
 
-hgemm_status_t ensure_splitk_workspace(Ctx* c, size_t partial_bytes, size_t n_tiles, cudaStream_t s) {
+// Partial sums and tickets shared by split-K and stream-K launches of a handle.
+hgemm_status_t ensure_workspace(Ctx* c, size_t partial_bytes, size_t n_tiles, cudaStream_t s) {
   if (c->partials_bytes < partial_bytes) {
     if (c->partials) cudaFree(c->partials);
     c->partials = nullptr;
@@ -277,10 +307,28 @@ uint64_t hgemm_encode_smem_desc(uint32_t smem_addr, uint32_t lbo_bytes, uint32_t
 
 hgemm_status_t hgemm_plan(int64_t M, int64_t N, int64_t K, hgemm_layout_t layout, hgemm_dtype_t in_dtype,
                           hgemm_dtype_t acc_dtype, hgemm_dtype_t out_dtype, int32_t num_sms, int32_t variant,
-                          int32_t group_m, hgemm_plan_t* plan) {
-  if (!plan) return HGEMM_ERR_INVALID_ARG;
+                          int32_t group_m, int32_t stream_k, hgemm_plan_t* plan) {
+  if (!plan || group_m < 0 || stream_k < 0 || stream_k > 1) return HGEMM_ERR_INVALID_ARG;
   return make_plan(M, N, K, layout, in_dtype, acc_dtype, out_dtype, num_sms, kDefaultSmemOptin, nullptr, variant,
-                   group_m, 0, plan);
+                   group_m, 0, stream_k != 0, plan);
+}
+
+hgemm_status_t hgemm_plan_work_item(const hgemm_plan_t* plan, int32_t cluster, int32_t index, int32_t* tile,
+                                    int32_t* kb0, int32_t* kb1, int32_t* slot) {
+  if (!plan || !tile || !kb0 || !kb1 || !slot || plan->variant == HGEMM_VARIANT_SPLITK || plan->cta_group < 1 ||
+      index < 0)
+    return HGEMM_ERR_INVALID_ARG;
+  const int32_t nclusters = plan->grid / plan->cta_group;
+  if (cluster < 0 || cluster >= nclusters) return HGEMM_ERR_INVALID_ARG;
+  WorkIter it(cluster, nclusters, plan->dp_tiles, plan->sk_units, plan->k_blocks);
+  WorkItem w;
+  for (int32_t i = 0; i <= index; ++i)
+    if (!it.next(w)) return HGEMM_ERR_INVALID_ARG;
+  *tile = w.tile;
+  *kb0 = w.kb0;
+  *kb1 = w.kb1;
+  *slot = w.slot;
+  return HGEMM_OK;
 }
 
 hgemm_status_t hgemm_plan_tile(const hgemm_plan_t* plan, int32_t t, int32_t* tile_m_idx, int32_t* tile_n_idx) {
@@ -349,6 +397,7 @@ hgemm_status_t hgemm_destroy(hgemm_handle_t h) {
   cudaError_t e = cudaDeviceSynchronize();
   if (h->partials) cudaFree(h->partials);
   if (h->tickets) cudaFree(h->tickets);
+  if (h->trace) cudaFree(h->trace);
   if (h->status) cudaFree(h->status);
   cudaSetDevice(prev);
   delete h;
@@ -378,6 +427,29 @@ hgemm_status_t hgemm_set_option(hgemm_handle_t h, int32_t option, int64_t value)
       if (value < 0 || value > 65536) return HGEMM_ERR_INVALID_ARG;
       h->max_ctas = (int)value;
       return HGEMM_OK;
+    case HGEMM_OPT_STREAM_K:
+      if (value < 0 || value > 1) return HGEMM_ERR_INVALID_ARG;
+      h->stream_k = value != 0;
+      return HGEMM_OK;
+    case HGEMM_OPT_TRACE: {
+      if (value < 0 || value > (int64_t)1 << 26) return HGEMM_ERR_INVALID_ARG;
+      if (h->trace) {
+        cudaDeviceSynchronize();
+        cudaFree(h->trace);
+        h->trace = nullptr;
+        h->trace_capacity = 0;
+      }
+      if (value == 0) return HGEMM_OK;
+      const size_t bytes = sizeof(TraceBuf) + (size_t)value * sizeof(TraceRecord);
+      if (cudaMalloc(reinterpret_cast<void**>(&h->trace), bytes) != cudaSuccess) {
+        h->trace = nullptr;
+        return HGEMM_ERR_OOM;
+      }
+      const unsigned long long head[2] = {0ull, (unsigned long long)value};
+      if (cudaMemcpy(h->trace, head, sizeof(head), cudaMemcpyHostToDevice) != cudaSuccess) return HGEMM_ERR_CUDA;
+      h->trace_capacity = value;
+      return HGEMM_OK;
+    }
   }
   return HGEMM_ERR_INVALID_ARG;
 }
@@ -401,7 +473,7 @@ hgemm_status_t hgemm_run(hgemm_handle_t h, const void* A, const void* B, void* C
 
   hgemm_plan_t p;
   st = make_plan(M, N, K, layout, in_dtype, acc_dtype, out_dtype, h->sm_count, h->smem_optin, h->capacity,
-                 h->force_variant, h->group_m, h->max_ctas, &p);
+                 h->force_variant, h->group_m, h->max_ctas, h->stream_k, &p);
   if (st != HGEMM_OK) return st;
 
   if (p.variant == HGEMM_VARIANT_SPLITK) {
@@ -411,7 +483,7 @@ hgemm_status_t hgemm_run(hgemm_handle_t h, const void* A, const void* B, void* C
         !encode_2d(&tmX, in_dtype, A, (uint64_t)K, (uint64_t)M, 64, (uint32_t)mma_n))
       return HGEMM_ERR_CUDA;
     const size_t partial_bytes = (size_t)p.grid * 2 * 128 * (size_t)mma_n * sizeof(float);
-    st = ensure_splitk_workspace(h, partial_bytes, (size_t)p.num_tiles, s);
+    st = ensure_workspace(h, partial_bytes, (size_t)p.num_tiles, s);
     if (st != HGEMM_OK) return st;
     if (p.smem_bytes > h->splitk_prepared_smem) return HGEMM_ERR_UNSUPPORTED;
     SplitKArgs args;
@@ -431,6 +503,7 @@ hgemm_status_t hgemm_run(hgemm_handle_t h, const void* A, const void* B, void* C
     args.partials = h->partials;
     args.tickets = h->tickets;
     args.C = C;
+    args.trace = h->trace;
     return cuda_status(splitk_launch(tmW, tmX, args, p.grid, p.smem_bytes, s));
   }
 
@@ -461,7 +534,37 @@ hgemm_status_t hgemm_run(hgemm_handle_t h, const void* A, const void* B, void* C
   args.inject = h->inject;
   args.timeout_ns = h->timeout_ns;
   args.status = h->status;
+  args.trace = h->trace;
+  args.dp_tiles = p.dp_tiles;
+  args.sk_units = p.sk_units;
+  args.partials = nullptr;
+  args.tickets = nullptr;
+  if (p.stream_k) {
+    const size_t clusters = (size_t)(p.grid / info.cta_group);
+    const size_t partial_bytes = clusters * 2 * (size_t)info.cta_group * (size_t)info.block_n * 128 * sizeof(float);
+    // two counters per tile and CTA of the pair: arrivals, then publications
+    st = ensure_workspace(h, partial_bytes, (size_t)p.num_tiles * (size_t)info.cta_group * 2, s);
+    if (st != HGEMM_OK) return st;
+    args.partials = h->partials;
+    args.tickets = h->tickets;
+  }
   return cuda_status(dense_launch(kind, tmA, tmB, tmC, args, p.grid, s));
+}
+
+hgemm_status_t hgemm_trace_read(hgemm_handle_t h, hgemm_trace_record_t* out, int64_t capacity, int64_t* n_events) {
+  static_assert(sizeof(hgemm_trace_record_t) == sizeof(TraceRecord), "trace record layout");
+  if (!h || !h->trace || capacity < 0 || (capacity > 0 && !out) || !n_events) return HGEMM_ERR_INVALID_ARG;
+  cudaError_t e = cudaDeviceSynchronize();
+  unsigned long long count = 0;
+  if (e == cudaSuccess) e = cudaMemcpy(&count, h->trace, sizeof(count), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_status(e);
+  *n_events = (int64_t)count;
+  int64_t n = (int64_t)count;
+  if (n > h->trace_capacity) n = h->trace_capacity;
+  if (n > capacity) n = capacity;
+  if (n > 0) e = cudaMemcpy(out, h->trace->rec, (size_t)n * sizeof(TraceRecord), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemset(h->trace, 0, sizeof(unsigned long long));
+  return cuda_status(e);
 }
 
 hgemm_status_t hgemm_sync_status(hgemm_handle_t h, void* stream, int32_t* detail) {

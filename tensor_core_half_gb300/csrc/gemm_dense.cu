@@ -85,6 +85,7 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t bars = base + S::BAR_OFF;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + S::MISC_OFF);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(gbase + S::MISC_OFF + 4);
+  volatile int32_t* ticket_slot = reinterpret_cast<volatile int32_t*>(gbase + S::MISC_OFF + 8);
 
   auto full_bar = [&](int s) -> uint32_t { return bars + 8u * s; };
   auto empty_bar = [&](int s) -> uint32_t { return bars + 8u * (STAGES + s); };
@@ -132,6 +133,12 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_after();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
   bool aborted = false;
+  // The prologue above touched no global memory; from here on the previous
+  // kernel in the stream (launched with programmatic serialisation) must be done.
+  pdl_launch_dependents();
+  pdl_wait_prior_grid();
+  TraceBuf* const tb = args.trace;
+  if (threadIdx.x == 0) trace_event(tb, 0, kTraceKernelBegin, -1, cluster);
 
   if (warp == 0) {
     // ------------------------------------------------- TMA producer ----
@@ -141,11 +148,14 @@ __global__ void __launch_bounds__(192, 1)
       int64_t issued = 0;
       bool ok = true;
       const uint32_t full_rank0 = (CG == 2) ? mapa_shared(full_bar(0), 0) : full_bar(0);
-      for (int t = cluster; ok && t < args.num_tiles; t += nclusters) {
-        const TileCoord tc = tile_coord(t, args.tiles_m, args.tiles_n, args.group_m);
+      WorkIter it(cluster, nclusters, args.dp_tiles, args.sk_units, args.k_blocks);
+      WorkItem w;
+      while (ok && it.next(w)) {
+        trace_event(tb, kRoleProducer, kTraceItemBegin, w.tile, w.kb0);
+        const TileCoord tc = tile_coord(w.tile, args.tiles_m, args.tiles_n, args.group_m);
         const int m_row = tc.m * (S::BM * CG) + (int)rank * S::BM;
         const int n_row = tc.n * BN + (int)rank * S::B_ROWS;
-        for (int kb = 0; kb < args.k_blocks; ++kb) {
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
           if (!mbar_wait<kCS>(empty_bar(stage), phase ^ 1u, ctl)) {
             ok = false;
             break;
@@ -185,6 +195,7 @@ __global__ void __launch_bounds__(192, 1)
             phase ^= 1u;
           }
         }
+        trace_event(tb, kRoleProducer, kTraceItemEnd, w.tile, w.kb1);
       }
       if (!ok) {
         report_timeout(args.status, kRoleProducer, abort_flag);
@@ -217,15 +228,18 @@ __global__ void __launch_bounds__(192, 1)
       const uint32_t b_step = args.b_mn_major ? (kMNMajorStepBytes >> 4) : (kKMajorStepBytes >> 4);
       const uint32_t b_lbo = args.b_mn_major ? kMNMajorLBO : 16u;
       const uint32_t b_sbo = args.b_mn_major ? kMNMajorSBO : kKMajorSBO;
-      for (int t = cluster; ok && t < args.num_tiles; t += nclusters) {
+      WorkIter it(cluster, nclusters, args.dp_tiles, args.sk_units, args.k_blocks);
+      WorkItem w;
+      while (ok && it.next(w)) {
         // Wait until the epilogue has drained this accumulator buffer.
         if (!mbar_wait<kCS>(tempty_bar(acc), acc_phase ^ 1u, ctl)) {
           ok = false;
           break;
         }
         tc_fence_after();
+        trace_event(tb, kRoleMma, kTraceItemBegin, w.tile, w.kb0);
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-        for (int kb = 0; kb < args.k_blocks; ++kb) {
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
           if (!mbar_wait<kCS>(full_bar(stage), phase, ctl)) {
             ok = false;
             break;
@@ -238,7 +252,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
           for (int kk = 0; kk < S::BK / 16; ++kk) {
             mma_f16<CG>(d_tmem, a_desc + (uint64_t)(kk * (kKMajorStepBytes >> 4)), b_desc + (uint64_t)(kk * b_step),
-                        args.idesc, (uint32_t)((kb | kk) != 0));
+                        args.idesc, (uint32_t)((kb != w.kb0) || (kk != 0)));
           }
           tc_commit_cg<CG>(empty_bar(stage), (uint16_t)0x3);  // frees the stage once these MMAs finish
           if (++stage == STAGES) {
@@ -248,6 +262,7 @@ __global__ void __launch_bounds__(192, 1)
         }
         if (!ok) break;
         tc_commit_cg<CG>(tfull_bar(acc), (uint16_t)0x3);  // accumulator ready for the epilogue
+        trace_event(tb, kRoleMma, kTraceItemEnd, w.tile, w.kb1);
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
       }
@@ -267,76 +282,177 @@ __global__ void __launch_bounds__(192, 1)
     // ----------------------------------------------------- epilogue ----
     const int q = warp & 3;   // TMEM lane quarter this warp may access
     const int ew = warp - 2;  // staging slot
+    const int row = q * 32 + (int)lane;  // row of this thread within the CTA's 128 rows
     int acc = 0;
     uint32_t acc_phase = 0;
     uint32_t nstores = 0;
     bool ok = true;
     const bool out_bf16 = args.out_bf16 != 0;
-    for (int t = cluster; t < args.num_tiles; t += nclusters) {
-      bool got = mbar_wait<kCS>(tfull_bar(acc), acc_phase, ctl);
-      got = __all_sync(0xffffffffu, got);
-      if (!got) {
+    const bool acc_f16 = args.acc_f16 != 0;
+
+    // 64 accumulator columns of this thread's row, as fp32.
+    auto load_chunk = [&](uint32_t t_row, int c, float (&f)[64]) {
+      uint32_t v[64];
+      tmem_ld_x32(t_row + (uint32_t)(c * 64), v);
+      tmem_ld_x32(t_row + (uint32_t)(c * 64 + 32), v + 32);
+      tmem_ld_wait();
+      if (!acc_f16) {
+#pragma unroll
+        for (int i = 0; i < 64; ++i) f[i] = __uint_as_float(v[i]);
+      } else {
+        // fp16 accumulators occupy one 32-bit TMEM column each, in the low half.
+#pragma unroll
+        for (int i = 0; i < 64; ++i) f[i] = __half2float(__ushort_as_half((unsigned short)(v[i] & 0xFFFFu)));
+      }
+    };
+
+    // Round 64 columns to the output type and store them (warp: 32 rows x 64 columns).
+    auto emit_chunk = [&](const float (&f)[64], int m0, int nc) {
+      if (!(m0 < args.M && nc < args.N)) return;  // warp-uniform; TMA clips partial boxes
+      uint32_t p[32];
+      if (out_bf16) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) p[i] = pack_f32x2_to_bf16x2(f[2 * i], f[2 * i + 1]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) p[i] = pack_f32x2_to_f16x2(f[2 * i], f[2 * i + 1]);
+      }
+      const uint32_t buf = epi + (uint32_t)(ew * 2 + (int)(nstores & 1u)) * S::EPI_BOX_BYTES;
+      if (lane == 0) bulk_wait_read<1>();  // the store that last used this buffer has read it
+      __syncwarp();
+      const uint32_t srow = buf + lane * 128u;
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        st_shared_v4(srow + ((uint32_t)(j ^ (int)(lane & 7u)) << 4), p[4 * j], p[4 * j + 1], p[4 * j + 2],
+                     p[4 * j + 3]);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(&tmC, buf, nc, m0);
+        bulk_commit();
+      }
+      ++nstores;
+    };
+
+    auto release_tmem = [&](int b) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if constexpr (CG == 1)
+          mbar_arrive(tempty_bar(b));
+        else
+          mbar_arrive_cluster(mapa_shared(tempty_bar(b), 0));
+      }
+    };
+
+    // Stream-K partial of cluster c, slot s, this CTA: BN/4 groups of 4 columns,
+    // each [128 rows] of float4, so a warp's accesses are 512 contiguous bytes.
+    auto partial_of = [&](int64_t c, int s) -> float4* {
+      return reinterpret_cast<float4*>(args.partials + (((c * 2 + s) * CG + rank) * (int64_t)BN * 128));
+    };
+
+    WorkIter it(cluster, nclusters, args.dp_tiles, args.sk_units, args.k_blocks);
+    WorkItem w;
+    while (it.next(w)) {
+      const bool got = mbar_wait<kCS>(tfull_bar(acc), acc_phase, ctl);
+      // The four epilogue warps meet at named barriers, so they give up together.
+      if (named_bar_or(2, 128, !got)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const TileCoord tc = tile_coord(t, args.tiles_m, args.tiles_n, args.group_m);
+      const bool tracer = threadIdx.x == 64;
+      if (tracer) trace_event(tb, kRoleEpilogue, kTraceItemBegin, w.tile, w.slot);
+      const TileCoord tc = tile_coord(w.tile, args.tiles_m, args.tiles_n, args.group_m);
       const int m0 = tc.m * (S::BM * CG) + (int)rank * S::BM + q * 32;  // first C row of this warp
       const int n0 = tc.n * BN;
       const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+      if (w.slot < 0) {
 #pragma unroll 1
-      for (int c = 0; c < BN / 64; ++c) {
-        uint32_t p[32];
-        if (!args.acc_f16) {
-          uint32_t v[64];
-          tmem_ld_x32(t_row + (uint32_t)(c * 64), v);
-          tmem_ld_x32(t_row + (uint32_t)(c * 64 + 32), v + 32);
-          tmem_ld_wait();
-          if (out_bf16) {
+        for (int c = 0; c < BN / 64; ++c) {
+          float f[64];
+          load_chunk(t_row, c, f);
+          if (c == BN / 64 - 1) release_tmem(acc);  // all reads of this accumulator are done
+          emit_chunk(f, m0, n0 + c * 64);
+        }
+      } else {
+        // A piece of a stream-K tile.  The ticket comes first: the contributor
+        // that arrives last keeps its accumulator in TMEM and adds the other
+        // contributors' fp32 partials to it; every other contributor publishes
+        // its partial and bumps the tile's publication count.  The sum always
+        // runs over the contributors in K order, whoever arrives last, so the
+        // result does not depend on timing.
+        const int32_t tix = w.tile * CG + (int32_t)rank;
+        int32_t* const arrivals = args.tickets + tix;
+        int32_t* const pubs = args.tickets + (int64_t)args.num_tiles * CG + tix;
+        int64_t c_first, c_last;
+        sk_contributors(w.tile, args.dp_tiles, args.sk_units, args.k_blocks, nclusters, &c_first, &c_last);
+        const int32_t others = (int32_t)(c_last - c_first);
+        if (threadIdx.x == 64) *ticket_slot = atomicAdd(arrivals, 1);
+        named_bar_sync(1, 128);
+        const int32_t ticket = *ticket_slot;
+        named_bar_sync(1, 128);
+        if (ticket != others) {
+          float4* mine = partial_of(cluster, w.slot) + row;
+#pragma unroll 1
+          for (int c = 0; c < BN / 64; ++c) {
+            float f[64];
+            load_chunk(t_row, c, f);
+            if (c == BN / 64 - 1) release_tmem(acc);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) p[i] = pack_f32x2_to_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) p[i] = pack_f32x2_to_f16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+            for (int j = 0; j < 16; ++j)
+              mine[(c * 16 + j) * 128] = make_float4(f[4 * j], f[4 * j + 1], f[4 * j + 2], f[4 * j + 3]);
           }
+          named_bar_sync(1, 128);  // every row of the partial is written ...
+          if (threadIdx.x == 64) red_add_release_gpu(pubs, 1);  // ... before it is published
+          if (tracer) trace_event(tb, kRoleEpilogue, kTracePartialStored, w.tile, ticket);
         } else {
-          // fp16 accumulators occupy one 32-bit TMEM column each, in the low half.
-          uint32_t v[64];
-          tmem_ld_x32(t_row + (uint32_t)(c * 64), v);
-          tmem_ld_x32(t_row + (uint32_t)(c * 64 + 32), v + 32);
-          tmem_ld_wait();
+          if (threadIdx.x == 64) {
+            const bool all_in = wait_counter_geq(pubs, others, ctl);
+            if (!all_in) report_timeout(args.status, kRoleEpilogue, abort_flag);
+            *ticket_slot = all_in ? 1 : 0;
+          }
+          named_bar_sync(1, 128);  // the acquire above orders the partial reads below
+          const bool have_all = *ticket_slot != 0;
+#pragma unroll 1
+          for (int c = 0; c < BN / 64; ++c) {
+            float f[64];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) p[i] = f16x2_to_out((v[2 * i] & 0xFFFFu) | (v[2 * i + 1] << 16), out_bf16);
-        }
-        if (c == BN / 64 - 1) {
-          // All reads of this accumulator are done: hand it back to the MMA warp.
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) {
-            if constexpr (CG == 1)
-              mbar_arrive(tempty_bar(acc));
-            else
-              mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));
+            for (int j = 0; j < 64; ++j) f[j] = 0.0f;
+            for (int64_t cc = c_first; cc <= c_last; ++cc) {
+              if (cc == cluster) {
+                float own[64];
+                load_chunk(t_row, c, own);
+                if (c == BN / 64 - 1) release_tmem(acc);
+#pragma unroll
+                for (int j = 0; j < 64; ++j) f[j] += own[j];
+              } else if (have_all) {
+                const float4* src =
+                    partial_of(cc, sk_slot_of(cc, w.tile, args.dp_tiles, args.sk_units, args.k_blocks, nclusters)) +
+                    row;
+                float4 g[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) g[j] = __ldcg(src + (c * 16 + j) * 128);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                  f[4 * j] += g[j].x;
+                  f[4 * j + 1] += g[j].y;
+                  f[4 * j + 2] += g[j].z;
+                  f[4 * j + 3] += g[j].w;
+                }
+              }
+            }
+            emit_chunk(f, m0, n0 + c * 64);
+          }
+          if (tracer) trace_event(tb, kRoleEpilogue, kTraceReduced, w.tile, others + 1);
+          if (threadIdx.x == 64) {  // ready for the next launch
+            *arrivals = 0;
+            *pubs = 0;
           }
         }
-        const int nc = n0 + c * S::EPI_BOX_COLS;
-        if (m0 < args.M && nc < args.N) {  // warp-uniform; rows/cols past the edge are clipped by TMA
-          const uint32_t buf = epi + (uint32_t)(ew * 2 + (int)(nstores & 1u)) * S::EPI_BOX_BYTES;
-          if (lane == 0) bulk_wait_read<1>();  // the store that last used this buffer has read it
-          __syncwarp();
-          const uint32_t row = buf + lane * 128u;
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            st_shared_v4(row + ((uint32_t)(j ^ (int)(lane & 7u)) << 4), p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_2d(&tmC, buf, nc, m0);
-            bulk_commit();
-          }
-          ++nstores;
-        }
+        named_bar_sync(1, 128);  // ticket_slot is reused by the next item
       }
+      if (tracer) trace_event(tb, kRoleEpilogue, kTraceItemEnd, w.tile, w.slot);
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
@@ -349,6 +465,7 @@ __global__ void __launch_bounds__(192, 1)
   }
 
   // --------------------------------------------------------- teardown ----
+  if (threadIdx.x == 0) trace_event(tb, 0, kTraceKernelEnd, -1, cluster);
   if constexpr (CG == 2) {
     // In a pair, the peer's loads signal CTA 0 and CTA 0's MMAs read the peer's
     // shared memory; after a give-up, leave time for copies still in flight.
@@ -403,8 +520,10 @@ cudaError_t dense_prepare(DenseKind kind) {
   return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, info.smem_bytes);
 }
 
+// Launch configuration: cluster shape for the CTA-pair kernel, and programmatic
+// stream serialisation so that back-to-back GEMMs overlap launch and prologue.
 static void fill_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, const DenseKindInfo& info, int grid,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, bool pdl) {
   cfg = cudaLaunchConfig_t{};
   cfg.gridDim = dim3((unsigned)grid, 1, 1);
   cfg.blockDim = dim3((unsigned)info.threads, 1, 1);
@@ -413,11 +532,16 @@ static void fill_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, cons
   cfg.attrs = attr;
   cfg.numAttrs = 0;
   if (info.cta_group > 1) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)info.cta_group;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.numAttrs = 1;
+    attr[cfg.numAttrs].id = cudaLaunchAttributeClusterDimension;
+    attr[cfg.numAttrs].val.clusterDim.x = (unsigned)info.cta_group;
+    attr[cfg.numAttrs].val.clusterDim.y = 1;
+    attr[cfg.numAttrs].val.clusterDim.z = 1;
+    ++cfg.numAttrs;
+  }
+  if (pdl) {
+    attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
+    ++cfg.numAttrs;
   }
 }
 
@@ -433,8 +557,8 @@ cudaError_t dense_max_active_clusters(DenseKind kind, int* clusters) {
     return e;
   }
   cudaLaunchConfig_t cfg;
-  cudaLaunchAttribute attr[1];
-  fill_config(cfg, attr, info, info.cta_group * 64, nullptr);
+  cudaLaunchAttribute attr[2];
+  fill_config(cfg, attr, info, info.cta_group * 64, nullptr, false);
   return cudaOccupancyMaxActiveClusters(clusters, dense_fn(kind), &cfg);
 }
 
@@ -442,8 +566,8 @@ cudaError_t dense_launch(DenseKind kind, const CUtensorMap& tmA, const CUtensorM
                          const DenseArgs& args, int grid_ctas, cudaStream_t stream) {
   const DenseKindInfo info = dense_kind_info(kind);
   cudaLaunchConfig_t cfg;
-  cudaLaunchAttribute attr[1];
-  fill_config(cfg, attr, info, grid_ctas, stream);
+  cudaLaunchAttribute attr[2];
+  fill_config(cfg, attr, info, grid_ctas, stream, true);
   switch (kind) {
 #define X(KIND, CG, BN, ST) \
   case KIND:                \

@@ -144,6 +144,12 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+  // The prologue above touched no global memory; from here on the previous
+  // kernel in the stream (launched with programmatic serialisation) must be done.
+  pdl_launch_dependents();
+  pdl_wait_prior_grid();
+  TraceBuf* const tb = args.trace;
+  if (threadIdx.x == 0) trace_event(tb, 0, kTraceKernelBegin, -1, (int32_t)begin);
 
   if (warp == 0) {
     // ---------------------------------------------------- TMA producer ----
@@ -154,6 +160,7 @@ __global__ void __launch_bounds__(192, 1)
       bool ok = true;
       for (int64_t u = begin; ok && u < end;) {
         const Segment sg = segment_at(u, end, args.k_blocks, begin);
+        trace_event(tb, kRoleProducer, kTraceItemBegin, sg.tile, sg.kb0);
         for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, ctl)) {
             ok = false;
@@ -176,6 +183,7 @@ __global__ void __launch_bounds__(192, 1)
         }
         u += sg.kb1 - sg.kb0;
       }
+      trace_event(tb, kRoleProducer, kTraceItemEnd, -1, (int32_t)issued);
       if (!ok) sk_report(args.status, kRoleProducer, abort_flag);
       for (int s = 0; s < stages; ++s) {
         if (issued <= s) break;
@@ -201,6 +209,7 @@ __global__ void __launch_bounds__(192, 1)
           break;
         }
         tc_fence_after();
+        trace_event(tb, kRoleMma, kTraceItemBegin, sg.tile, sg.kb0);
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * mma_n);
         for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
           if (!mbar_wait(full_bar(stage), phase, ctl)) {
@@ -225,6 +234,7 @@ __global__ void __launch_bounds__(192, 1)
         }
         if (!ok) break;
         tc_commit(tfull_bar(acc));
+        trace_event(tb, kRoleMma, kTraceItemEnd, sg.tile, sg.kb1);
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
         u += sg.kb1 - sg.kb0;
@@ -252,6 +262,7 @@ __global__ void __launch_bounds__(192, 1)
         break;
       }
       tc_fence_after();
+      if (threadIdx.x == 64) trace_event(tb, kRoleEpilogue, kTraceItemBegin, sg.tile, sg.kb0);
       float v[kSplitKMaxM];
       const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * mma_n);
 #pragma unroll
@@ -285,17 +296,16 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
         for (int j = 0; j < kSplitKMaxM / 4; ++j)
           if (j * 4 < mma_n) reinterpret_cast<float4*>(mine)[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-        __threadfence();
-        named_bar_sync(1, 128);
+        named_bar_sync(1, 128);  // every row of our partial is written before the ticket
         const int64_t u_first = (int64_t)sg.tile * args.k_blocks;
         const int64_t u_last = u_first + args.k_blocks - 1;
         const int64_t c_first = splitk_owner(u_first, args.units, G);
         const int64_t c_last = splitk_owner(u_last, args.units, G);
-        if (threadIdx.x == 64) *ticket_slot = atomicAdd(args.tickets + sg.tile, 1);
+        // acq_rel: publishes our partial and, for the last arriver, acquires the others'
+        if (threadIdx.x == 64) *ticket_slot = atom_add_acq_rel_gpu(args.tickets + sg.tile, 1);
         named_bar_sync(1, 128);
         const int32_t ticket = *ticket_slot;
         if (ticket == (int32_t)(c_last - c_first)) {
-          __threadfence();
           float s[kSplitKMaxM];
 #pragma unroll
           for (int m = 0; m < kSplitKMaxM; ++m) s[m] = 0.0f;
@@ -324,11 +334,13 @@ __global__ void __launch_bounds__(192, 1)
         }
         named_bar_sync(1, 128);  // ticket_slot is reused by the next segment
       }
+      if (threadIdx.x == 64) trace_event(tb, kRoleEpilogue, kTraceItemEnd, sg.tile, sg.kb1);
       u += sg.kb1 - sg.kb0;
     }
     if (!ok && lane == 0) sk_report(args.status, kRoleEpilogue, abort_flag);
   }
 
+  if (threadIdx.x == 0) trace_event(tb, 0, kTraceKernelEnd, -1, (int32_t)end);
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
@@ -343,8 +355,17 @@ cudaError_t splitk_prepare(int smem_bytes) {
 
 cudaError_t splitk_launch(const CUtensorMap& tmW, const CUtensorMap& tmX, const SplitKArgs& args, int grid,
                           int smem_bytes, cudaStream_t stream) {
-  splitk_gemm_kernel<<<grid, kThreads, (size_t)smem_bytes, stream>>>(tmW, tmX, args);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3((unsigned)kThreads, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)smem_bytes;
+  cfg.stream = stream;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // overlap launch with the previous kernel
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, splitk_gemm_kernel, tmW, tmX, args);
 }
 
 // ------------------------------------------------------------ zero fill ----

@@ -11,6 +11,30 @@ namespace hg {
 constexpr int32_t kStatusTimeout = 7;  // == HGEMM_ERR_TIMEOUT
 enum Role : int32_t { kRoleProducer = 1, kRoleMma = 2, kRoleEpilogue = 3, kRoleTeardown = 4 };
 
+// Intra-kernel event trace (HGEMM_OPT_TRACE): a device buffer of fixed-size
+// records appended with an atomic counter.  Kinds are listed in hgemm.h.
+struct TraceRecord {
+  uint64_t t_ns;     // %globaltimer
+  uint32_t cta;      // blockIdx.x
+  uint16_t role;     // Role
+  uint16_t kind;     // event kind
+  int32_t item;      // tile index (or -1)
+  int32_t value;     // kind-specific (k-block range start, ticket, ...)
+};
+enum TraceKind : uint16_t {
+  kTraceKernelBegin = 1,    // after setup (value: cluster or first unit)
+  kTraceKernelEnd = 2,      // before teardown
+  kTraceItemBegin = 3,      // a role starts a work item (value: first k-block, or slot for the epilogue)
+  kTraceItemEnd = 4,        // a role finishes it
+  kTracePartialStored = 5,  // stream-K partial published (value: ticket drawn)
+  kTraceReduced = 6,        // a split tile reduced and stored (value: contributors)
+};
+struct TraceBuf {
+  unsigned long long count;  // records requested (may exceed capacity)
+  unsigned long long capacity;
+  TraceRecord rec[1];
+};
+
 // Default limit of every bounded device-side wait.
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 // Limit used when draining in-flight copies after another role gave up.
@@ -20,6 +44,10 @@ constexpr uint64_t kDrainTimeoutNs = 2000000ull;
 struct DenseArgs {
   int32_t M, N, K;
   int32_t tiles_m, tiles_n, num_tiles, k_blocks, group_m;
+  int32_t dp_tiles;  // tiles computed over the whole K range (round-robin), before the stream-K range
+  int64_t sk_units;  // (num_tiles - dp_tiles) * k_blocks, split evenly over the clusters
+  float* partials;   // stream-K partials [clusters][2][cta_group][BN/4][128] float4 (null if sk_units == 0)
+  int32_t* tickets;  // [2][num_tiles * cta_group] arrivals, publications; all zero between launches
   uint32_t idesc;
   int32_t b_mn_major;      // NN layout: B tile is MN-major in shared memory
   int32_t acc_f16;         // fp16 accumulators in tensor memory (one per 32-bit column, low half)
@@ -27,6 +55,7 @@ struct DenseArgs {
   int32_t inject;          // test-only fault injection (HGEMM_OPT_INJECT_FAULT)
   uint64_t timeout_ns;
   int32_t* status;
+  TraceBuf* trace;         // null unless tracing
 };
 
 enum DenseKind : int { kDense1Sm128 = 0, kDense1Sm256 = 1, kDense2Sm256 = 2 };
@@ -59,6 +88,7 @@ struct SplitKArgs {
   float* partials;   // [grid][2][128][mma_n] fp32
   int32_t* tickets;  // [n_tiles], all zero between launches
   void* C;           // [M][N] row-major
+  TraceBuf* trace;   // null unless tracing
 };
 
 constexpr int kSplitKMaxM = 64;

@@ -181,5 +181,6 @@ extern "C" hgemm_status_t hgemm_run_splitk_noalloc(const void* A, const void* B,
   args.tickets = reinterpret_cast<int32_t*>(d->scratch + kStatusBytes);
   args.partials = reinterpret_cast<float*>(d->scratch + kPartialOffset);
   args.C = C;
+  args.trace = nullptr;
   return hg::splitk_launch(tmW, tmX, args, (int)grid, smem, s) == cudaSuccess ? HGEMM_OK : HGEMM_ERR_CUDA;
 }

@@ -42,6 +42,13 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// Programmatic dependent launch: let the next kernel of the stream start its
+// prologue now / wait until the previous kernel's memory operations are visible.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait_prior_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- cluster ----
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
@@ -334,6 +341,58 @@ __device__ __forceinline__ uint32_t pack_f32x2_to_f16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
+}
+
+// ----------------------------------------------------- global counters ----
+__device__ __forceinline__ int32_t ld_acquire_gpu(const int32_t* p) {
+  int32_t v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Add with release semantics at GPU scope: the writes that happen before it
+// (including other threads' writes ordered by a CTA barrier) become visible to
+// a thread that acquires the new value.
+__device__ __forceinline__ void red_add_release_gpu(int32_t* p, int32_t v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Fetch-and-add with acquire and release semantics at GPU scope.
+__device__ __forceinline__ int32_t atom_add_acq_rel_gpu(int32_t* p, int32_t v) {
+  int32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+// Bounded wait until *p >= target (another CTA's release-ordered increments).
+static __device__ __noinline__ bool wait_counter_geq(const int32_t* p, int32_t target, WaitCtl ctl) {
+  if (ld_acquire_gpu(p) >= target) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    __nanosleep(64);
+    if (ld_acquire_gpu(p) >= target) return true;
+    if ((i & 15u) == 0) {
+      if (ctl.abort_flag != nullptr && *ctl.abort_flag != 0u) return false;
+      if (globaltimer_ns() - t0 > ctl.timeout_ns) return false;
+    }
+  }
+}
+
+// ------------------------------------------------------------ tracing ----
+// Appends one event to a trace buffer (see kernels.h); no-op for a null buffer.
+template <class Buf>
+__device__ __forceinline__ void trace_event(Buf* tb, uint16_t role, uint16_t kind, int32_t item, int32_t value) {
+  if (tb == nullptr) return;
+  const unsigned long long i = atomicAdd(&tb->count, 1ull);
+  if (i < tb->capacity) {
+    auto& r = tb->rec[i];
+    r.t_ns = globaltimer_ns();
+    r.cta = blockIdx.x;
+    r.role = role;
+    r.kind = kind;
+    r.item = item;
+    r.value = value;
+  }
 }
 
 }  // namespace hg

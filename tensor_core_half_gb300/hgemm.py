@@ -55,6 +55,8 @@ HGEMM_OPT_TIMEOUT_NS = 2
 HGEMM_OPT_INJECT_FAULT = 3
 HGEMM_OPT_GROUP_M = 4
 HGEMM_OPT_MAX_CTAS = 5
+HGEMM_OPT_STREAM_K = 6
+HGEMM_OPT_TRACE = 7
 
 LAYOUTS = {"TN": HGEMM_LAYOUT_TN, "NN": HGEMM_LAYOUT_NN}
 DTYPES = {"f16": HGEMM_F16, "bf16": HGEMM_BF16, "f32": HGEMM_F32}
@@ -65,7 +67,9 @@ VARIANTS = {"auto": HGEMM_VARIANT_AUTO, "1sm128": HGEMM_VARIANT_1SM_128x128, "1s
 class hgemm_plan_t(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "variant", "cta_group", "tile_m", "tile_n", "block_k", "stages", "tiles_m", "tiles_n", "num_tiles",
-        "k_blocks", "grid", "group_m", "smem_bytes", "tmem_cols")] + [("workspace_bytes", ctypes.c_int64)]
+        "k_blocks", "grid", "group_m", "smem_bytes", "tmem_cols")] + [
+        ("workspace_bytes", ctypes.c_int64), ("dp_tiles", ctypes.c_int32), ("stream_k", ctypes.c_int32),
+        ("sk_units", ctypes.c_int64)]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -90,7 +94,10 @@ _lib.hgemm_set_option.argtypes = [_vp, _i32, _i64]
 _lib.hgemm_status_string.restype = ctypes.c_char_p
 _lib.hgemm_status_string.argtypes = [_i32]
 _lib.hgemm_plan.restype = _i32
-_lib.hgemm_plan.argtypes = [_i64, _i64, _i64, _i32, _i32, _i32, _i32, _i32, _i32, _i32, ctypes.POINTER(hgemm_plan_t)]
+_lib.hgemm_plan.argtypes = [_i64, _i64, _i64, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
+                            ctypes.POINTER(hgemm_plan_t)]
+_lib.hgemm_plan_work_item.restype = _i32
+_lib.hgemm_plan_work_item.argtypes = [ctypes.POINTER(hgemm_plan_t), _i32, _i32] + [ctypes.POINTER(_i32)] * 4
 _lib.hgemm_plan_tile.restype = _i32
 _lib.hgemm_plan_tile.argtypes = [ctypes.POINTER(hgemm_plan_t), _i32, ctypes.POINTER(_i32), ctypes.POINTER(_i32)]
 _lib.hgemm_plan_splitk_range.restype = _i32
@@ -104,6 +111,15 @@ _lib.hgemm_version.restype = _i32
 _lib.hgemm_version.argtypes = []
 _lib.hgemm_run_splitk_noalloc.restype = _i32
 _lib.hgemm_run_splitk_noalloc.argtypes = [_vp, _vp, _vp, _i64, _i64, _i64, _i32, _i32, _vp]
+
+
+class hgemm_trace_record_t(ctypes.Structure):
+    _fields_ = [("t_ns", ctypes.c_uint64), ("cta", ctypes.c_uint32), ("role", ctypes.c_uint16),
+                ("kind", ctypes.c_uint16), ("item", ctypes.c_int32), ("value", ctypes.c_int32)]
+
+
+_lib.hgemm_trace_read.restype = _i32
+_lib.hgemm_trace_read.argtypes = [_vp, ctypes.POINTER(hgemm_trace_record_t), _i64, ctypes.POINTER(_i64)]
 
 
 class HgemmError(RuntimeError):
@@ -163,11 +179,18 @@ def hgemm_set_option(h, option, value) -> int:
 
 
 def hgemm_plan(M, N, K, layout=HGEMM_LAYOUT_TN, in_dtype=HGEMM_BF16, acc_dtype=HGEMM_F32, out_dtype=HGEMM_BF16,
-               num_sms=152, variant=HGEMM_VARIANT_AUTO, group_m=0):
+               num_sms=152, variant=HGEMM_VARIANT_AUTO, group_m=0, stream_k=1):
     p = hgemm_plan_t()
     st = _lib.hgemm_plan(int(M), int(N), int(K), int(layout), int(in_dtype), int(acc_dtype), int(out_dtype),
-                         int(num_sms), int(variant), int(group_m), ctypes.byref(p))
+                         int(num_sms), int(variant), int(group_m), int(stream_k), ctypes.byref(p))
     return int(st), p
+
+
+def hgemm_plan_work_item(plan, cluster, index):
+    t, a, b, s = _i32(), _i32(), _i32(), _i32()
+    st = _lib.hgemm_plan_work_item(ctypes.byref(plan), int(cluster), int(index), ctypes.byref(t), ctypes.byref(a),
+                                   ctypes.byref(b), ctypes.byref(s))
+    return int(st), t.value, a.value, b.value, s.value
 
 
 def hgemm_plan_tile(plan, t):
@@ -195,6 +218,16 @@ def hgemm_run_splitk_noalloc(A, B, C, M, N, K, in_dtype, out_dtype, stream=0) ->
     """Skinny-M product with scratch in a fixed device array: no allocation,
     no handle (for callers that cannot allocate device memory)."""
     return int(_lib.hgemm_run_splitk_noalloc(A, B, C, int(M), int(N), int(K), int(in_dtype), int(out_dtype), stream))
+
+
+def hgemm_trace_read(h, capacity):
+    """Returns (status, events recorded, list of (t_ns, cta, role, kind, item, value))."""
+    buf = (hgemm_trace_record_t * max(1, int(capacity)))()
+    n = _i64(0)
+    st = _lib.hgemm_trace_read(h, buf, int(capacity), ctypes.byref(n))
+    rows = [(r.t_ns, r.cta, r.role, r.kind, r.item, r.value) for r in buf[:min(int(capacity), n.value)]] \
+        if st == HGEMM_OK else []
+    return int(st), int(n.value), rows
 
 
 # ------------------------------------------------------ torch helpers ----

@@ -24,8 +24,9 @@ def h():
     handle.close()
 
 
-def run(h, a, b, M, N, K, layout, acc, out, variant="auto", C=None):
+def run(h, a, b, M, N, K, layout, acc, out, variant="auto", C=None, stream_k=1):
     h.set_option(hgemm.HGEMM_OPT_FORCE_VARIANT, hgemm.VARIANTS[variant])
+    h.set_option(hgemm.HGEMM_OPT_STREAM_K, stream_k)
     try:
         A, B = a.cuda(), b.cuda()
         if C is None:
@@ -36,6 +37,7 @@ def run(h, a, b, M, N, K, layout, acc, out, variant="auto", C=None):
         return workloads.bits(C.cpu())
     finally:
         h.set_option(hgemm.HGEMM_OPT_FORCE_VARIANT, hgemm.HGEMM_VARIANT_AUTO)
+        h.set_option(hgemm.HGEMM_OPT_STREAM_K, 1)
 
 
 @pytest.mark.parametrize("variant", ["auto"] + DENSE_VARIANTS)
@@ -138,9 +140,35 @@ def test_variants_agree_bitwise(h, layout):
     # is one tensor-core accumulation over K in the same order.
     M, N, K = 512, 512, 1024
     a, b, _, _ = parity.inputs(M, N, K, layout, "f16", ("uniform", -1.0, 1.0), 32)
-    outs = [run(h, a, b, M, N, K, layout, "f32", "f16", v) for v in DENSE_VARIANTS]
+    outs = [run(h, a, b, M, N, K, layout, "f32", "f16", v, stream_k=0) for v in DENSE_VARIANTS]
     for o in outs[1:]:
         assert np.array_equal(o, outs[0])
+
+
+@pytest.mark.parametrize("variant", DENSE_VARIANTS)
+@pytest.mark.parametrize("layout", ["TN", "NN"])
+@pytest.mark.parametrize("combo", [("bf16", "f32", "bf16"), ("f16", "f16", "f16")], ids=["bf16", "f16acc"])
+@pytest.mark.parametrize("M,N,K", [(1024, 1280, 1024), (768, 520, 4104), (256, 264, 200)])
+def test_stream_k_parity(h, M, N, K, combo, layout, variant):
+    # Tile counts that leave a partial last wave, so stream-K splits tiles.
+    fin, acc, out = combo
+    st, p = hgemm.hgemm_plan(M, N, K, hgemm.LAYOUTS[layout], hgemm.DTYPES[fin], hgemm.DTYPES[acc], hgemm.DTYPES[out],
+                             torch.cuda.get_device_properties(0).multi_processor_count, hgemm.VARIANTS[variant])
+    assert st == 0
+    a, b, ab, bb = parity.inputs(M, N, K, layout, fin, ("uniform", -1.0, 1.0), 61)
+    got = run(h, a, b, M, N, K, layout, acc, out, variant)
+    parity.check(got, ab, bb, M, N, K, layout, fin, acc, out)
+    again = run(h, a, b, M, N, K, layout, acc, out, variant)
+    assert np.array_equal(got, again)  # the fix-up order is fixed: run-to-run identical
+
+
+@pytest.mark.parametrize("variant", DENSE_VARIANTS)
+def test_stream_k_small_integers_bit_exact(h, variant):
+    M, N, K = 640, 640, 4096
+    a, b, ab, bb = parity.inputs(M, N, K, "TN", "bf16", ("int", -4, 4), 62)
+    got = run(h, a, b, M, N, K, "TN", "f32", "bf16", variant)
+    ref, _, _ = oracle.gemm(ab, bb, M, N, K, "TN", "bf16", "bf16")
+    assert np.array_equal(got, ref)
 
 
 @pytest.mark.parametrize("variant,M,N,K", [("2sm256", 300, 264, 200), ("1sm128", 130, 136, 72),

@@ -1,0 +1,67 @@
+"""The intra-kernel tracer records exactly the schedule the planner describes."""
+import collections
+
+import pytest
+import torch
+
+from tests import parity
+from tensor_core_half_gb300 import hgemm, trace
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("variant,M,N,K", [("2sm256", 1024, 1280, 1024), ("1sm128", 640, 1000, 4104),
+                                           ("splitk", 16, 4096, 4096)])
+def test_trace_matches_plan(variant, M, N, K):
+    with hgemm.Handle() as h:
+        h.set_option(hgemm.HGEMM_OPT_FORCE_VARIANT, hgemm.VARIANTS[variant])
+        h.set_option(hgemm.HGEMM_OPT_TRACE, 1 << 16)
+        a, b, _, _ = parity.inputs(M, N, K, "TN", "bf16", ("normal", 1.0), 71)
+        A, B = a.cuda(), b.cuda()
+        C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        h.run(A, B, C, layout="TN", acc="f32")
+        assert h.sync_status()[0] == hgemm.HGEMM_OK
+        st, n, rows = hgemm.hgemm_trace_read(h.h, 1 << 16)
+        assert st == hgemm.HGEMM_OK and n == len(rows) > 0
+        st2, n2, _ = hgemm.hgemm_trace_read(h.h, 16)
+        assert st2 == hgemm.HGEMM_OK and n2 == 0  # reading empties the buffer
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    st, p = hgemm.hgemm_plan(M, N, K, 0, hgemm.HGEMM_BF16, hgemm.HGEMM_F32, hgemm.HGEMM_BF16, sms,
+                             hgemm.VARIANTS[variant])
+    kinds = collections.Counter((r[2], r[3]) for r in rows)
+    assert kinds[(0, 1)] == p.grid and kinds[(0, 2)] == p.grid  # every CTA begins and ends
+    if variant == "splitk":
+        return
+    clusters = p.grid // p.cta_group
+    items, partials = 0, 0
+    for c in range(clusters):
+        i = 0
+        while True:
+            s, t, a0, b0, slot = hgemm.hgemm_plan_work_item(p, c, i)
+            if s != 0:
+                break
+            items += 1
+            partials += slot >= 0
+            i += 1
+    # producer and epilogue run in every CTA; the MMA issuer in one CTA per cluster
+    assert kinds[(1, 3)] == kinds[(1, 4)] == items * p.cta_group
+    assert kinds[(2, 3)] == kinds[(2, 4)] == items
+    assert kinds[(3, 3)] == kinds[(3, 4)] == items * p.cta_group
+    # every partial item either publishes its partial or, arriving last, reduces the tile
+    assert kinds[(3, 5)] + kinds[(3, 6)] == partials * p.cta_group
+    # each split tile is reduced once per CTA of the pair, by its last contributor
+    split_tiles = len({t for c in range(clusters) for t in _partial_tiles(p, c)})
+    assert kinds[(3, 6)] == split_tiles * p.cta_group
+    s = trace.summary(rows)
+    assert s["items"] == items * (1 + 2 * p.cta_group)
+
+
+def _partial_tiles(p, c):
+    i, out = 0, []
+    while True:
+        s, t, a0, b0, slot = hgemm.hgemm_plan_work_item(p, c, i)
+        if s != 0:
+            return out
+        if slot >= 0:
+            out.append(t)
+        i += 1

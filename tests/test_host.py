@@ -41,8 +41,8 @@ def test_null_handle_is_rejected():
     assert H.hgemm_destroy(None) == ST_OK
 
 
-def plan(M, N, K, layout=0, fin=1, acc=2, out=1, sms=152, variant=0, group_m=0):
-    return H.hgemm_plan(M, N, K, layout, fin, acc, out, sms, variant, group_m)
+def plan(M, N, K, layout=0, fin=1, acc=2, out=1, sms=152, variant=0, group_m=0, stream_k=1):
+    return H.hgemm_plan(M, N, K, layout, fin, acc, out, sms, variant, group_m, stream_k)
 
 
 @pytest.mark.parametrize("args,expect", [
@@ -70,6 +70,13 @@ def test_plan_variant_choice():
     assert st == ST_OK and p.variant == H.HGEMM_VARIANT_2SM_256x256 and p.cta_group == 2
     assert (p.tile_m, p.tile_n, p.tiles_m, p.tiles_n, p.num_tiles, p.k_blocks) == (256, 256, 16, 16, 256, 64)
     assert p.grid == 152 and p.tmem_cols == 512 and p.smem_bytes <= 232448
+    # 256 tiles over 76 pairs: two whole waves data-parallel, the rest stream-K
+    assert p.stream_k == 1 and p.dp_tiles == 152 and p.sk_units == (256 - 152) * 64
+    st, p = plan(4096, 4096, 4096, stream_k=0)
+    assert st == ST_OK and p.stream_k == 0 and p.dp_tiles == 256 and p.sk_units == 0 and p.workspace_bytes == 0
+    # a tile count that is a whole number of waves stays data-parallel
+    st, p = plan(256 * 76, 256, 4096)
+    assert st == ST_OK and p.variant == H.HGEMM_VARIANT_2SM_256x256 and p.stream_k == 0
     st, p = plan(16, 16384, 8192)
     assert st == ST_OK and p.variant == H.HGEMM_VARIANT_SPLITK and p.tile_n == 16 and p.num_tiles == 128
     assert p.grid == 152 and p.k_blocks == 128 and p.workspace_bytes > 0
@@ -160,3 +167,72 @@ def test_instruction_descriptor_bits(args, word):
 ])
 def test_shared_memory_descriptor_bits(args, word):
     assert H.hgemm_encode_smem_desc(*args) == word
+
+
+STREAMK_CASES = [(4096, 4096, 4096, 3), (2048, 2048, 2048, 3), (1000, 3000, 4104, 1), (1000, 3000, 4104, 3),
+                 (8192, 8192, 8192, 3), (256, 256, 4096, 3), (640, 1024, 2048, 2), (256, 512, 128, 3)]
+
+
+@pytest.mark.parametrize("M,N,K,variant", STREAMK_CASES)
+def test_work_lists_cover_every_unit_once(M, N, K, variant):
+    st, p = plan(M, N, K, variant=variant)
+    assert st == ST_OK
+    clusters = p.grid // p.cta_group
+    covered = {}
+    per_cluster = []
+    slots = {}
+    for c in range(clusters):
+        i, work = 0, 0
+        while True:
+            s, t, a, b, slot = H.hgemm_plan_work_item(p, c, i)
+            if s != ST_OK:
+                break
+            assert 0 <= t < p.num_tiles and 0 <= a < b <= p.k_blocks
+            if slot < 0:
+                assert (a, b) == (0, p.k_blocks)
+            else:
+                assert t >= p.dp_tiles and (a, b) != (0, p.k_blocks)
+                assert (c, slot) not in slots  # at most one partial per slot
+                slots[(c, slot)] = t
+            for kb in range(a, b):
+                assert (t, kb) not in covered
+                covered[(t, kb)] = c
+            work += b - a
+            i += 1
+        per_cluster.append(work)
+    assert len(covered) == p.num_tiles * p.k_blocks
+    if p.stream_k:
+        # every cluster does the same number of k-blocks, up to one
+        assert max(per_cluster) - min(per_cluster) <= 1
+        # a split tile's pieces come from consecutive clusters, in K order
+        for t in range(p.dp_tiles, p.num_tiles):
+            owners = [covered[(t, kb)] for kb in range(p.k_blocks)]
+            assert owners == sorted(owners)
+            assert set(owners) == set(range(owners[0], owners[-1] + 1))
+
+
+def test_work_list_arguments():
+    st, p = plan(4096, 4096, 4096)
+    assert H.hgemm_plan_work_item(p, -1, 0)[0] == ST_INV
+    assert H.hgemm_plan_work_item(p, p.grid // 2, 0)[0] == ST_INV
+    assert H.hgemm_plan_work_item(p, 0, -1)[0] == ST_INV
+    st, sp = plan(16, 16384, 8192)
+    assert H.hgemm_plan_work_item(sp, 0, 0)[0] == ST_INV  # split-K plans have no dense work list
+
+
+def test_trace_read_requires_tracing():
+    st, n, rows = H.hgemm_trace_read(None, 4)
+    assert st == ST_INV and rows == []
+
+
+def test_trace_summary_and_chrome_format():
+    from tensor_core_half_gb300 import trace
+    rows = [(1000, 0, 0, 1, -1, 0), (1100, 0, 1, 3, 5, 0), (1900, 0, 1, 4, 5, 64), (1200, 0, 2, 3, 5, 0),
+            (2000, 0, 2, 4, 5, 64), (2100, 0, 3, 3, 5, -1), (2600, 0, 3, 4, 5, -1), (2700, 0, 0, 2, -1, 0),
+            (1000, 1, 0, 1, -1, 1), (2900, 1, 0, 2, -1, 1)]
+    s = trace.summary(rows)
+    assert s["span_ns"] == 1900 and s["items"] == 3 and s["cta_end_ns"] == [1700, 1900]
+    assert s["busy_ns_per_cta"]["tma"] == 400.0
+    doc = trace.chrome_trace(rows)
+    names = sorted(e["name"] for e in doc["traceEvents"])
+    assert names.count("tile 5") == 3 and "kernel_end" in names
