@@ -303,19 +303,17 @@ def main():
 
     # ------------------------------------------------------ end to end ------
     e2e_steps = args.e2e_steps if args.e2e_steps is not None else max(3, min(args.steps, 50))
+    # End to end: the C-ABI call on HOST buffers (hgemm_run_host), which uploads
+    # A and B from page-locked memory and downloads C inside every step.
     a_pin = a_cpu.pin_memory()
     b_pin = b_cpu.pin_memory()
     c_pin = torch.empty((w.M, w.N), dtype=dt).pin_memory()
-    Ad, Bd, Cd = A[0], B[0], C[0]
 
     def e2e_step():
-        Ad.copy_(a_pin, non_blocking=True)
-        Bd.copy_(b_pin, non_blocking=True)
-        s = hgemm.hgemm_run(handle.h, Ad.data_ptr(), Bd.data_ptr(), Cd.data_ptr(), w.M, w.N, w.K, lay, fin, facc,
-                            fout, sp)
+        s = hgemm.hgemm_run_host(handle.h, a_pin.data_ptr(), b_pin.data_ptr(), c_pin.data_ptr(), w.M, w.N, w.K, lay,
+                                 fin, facc, fout, sp)
         if s != hgemm.HGEMM_OK:
-            raise hgemm.HgemmError(s, "hgemm_run (e2e)")
-        c_pin.copy_(Cd, non_blocking=True)
+            raise hgemm.HgemmError(s, "hgemm_run_host (e2e)")
 
     for _ in range(2):
         e2e_step()
@@ -343,7 +341,9 @@ def main():
     peaks, peak_src = load_peaks()
     timed_seconds = total_ms / 1e3
     if bound == "tensor":
-        sustained = timed_seconds > 1.0
+        # The sustained (power-capped) peak applies once the loop runs long enough
+        # for the power cap to engage, which the clock record shows.
+        sustained = timed_seconds > 1.0 or "sw_power_cap" in (clocks.get("reasons") or [])
         peak = peaks.get("bf16_tflops_sustained" if sustained else "bf16_tflops")
         achieved = (w.flops / 1e12) / (kernel_ms_avg / 1e3)
         roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
@@ -380,7 +380,7 @@ def main():
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_value, 3), "unit": unit, "h2d_bytes_per_step": int(in_bytes),
-                "d2h_bytes_per_step": int(c_bytes), "steps": e2e_steps},
+                "d2h_bytes_per_step": int(c_bytes), "steps": e2e_steps, "api": "hgemm_run_host"},
         "gpu_launches": args.steps,
         "clocks": clocks,
     }

@@ -49,6 +49,21 @@ struct Ctx {
   bool stream_k = true;
   TraceBuf* trace = nullptr;  // device trace buffer (HGEMM_OPT_TRACE)
   int64_t trace_capacity = 0;
+  // hgemm_run_host: two staging sets (double buffering across calls), three
+  // internal streams and the events that chain them.
+  struct HostStage {
+    void* A = nullptr;
+    void* B = nullptr;
+    void* C = nullptr;
+    size_t a_cap = 0, b_cap = 0, c_cap = 0;
+    cudaEvent_t ev_free = nullptr;  // recorded when the last copy out of this set is done
+    cudaEvent_t ev_a[8] = {};       // chunk i of A (and all of B) is on the device
+    cudaEvent_t ev_c[8] = {};       // chunk i of C is computed
+    bool used = false;
+  } stage[2];
+  int stage_next = 0;
+  cudaStream_t s_h2d = nullptr, s_compute = nullptr, s_d2h = nullptr;
+  cudaEvent_t ev_entry = nullptr, ev_done = nullptr;
   int capacity[3] = {0, 0, 0};  // resident clusters per dense kind
   int splitk_prepared_smem = 0;
 };
@@ -398,6 +413,21 @@ hgemm_status_t hgemm_destroy(hgemm_handle_t h) {
   if (h->partials) cudaFree(h->partials);
   if (h->tickets) cudaFree(h->tickets);
   if (h->trace) cudaFree(h->trace);
+  for (auto& st : h->stage) {
+    if (st.A) cudaFree(st.A);
+    if (st.B) cudaFree(st.B);
+    if (st.C) cudaFree(st.C);
+    if (st.ev_free) cudaEventDestroy(st.ev_free);
+    for (int i = 0; i < 8; ++i) {
+      if (st.ev_a[i]) cudaEventDestroy(st.ev_a[i]);
+      if (st.ev_c[i]) cudaEventDestroy(st.ev_c[i]);
+    }
+  }
+  if (h->s_h2d) cudaStreamDestroy(h->s_h2d);
+  if (h->s_compute) cudaStreamDestroy(h->s_compute);
+  if (h->s_d2h) cudaStreamDestroy(h->s_d2h);
+  if (h->ev_entry) cudaEventDestroy(h->ev_entry);
+  if (h->ev_done) cudaEventDestroy(h->ev_done);
   if (h->status) cudaFree(h->status);
   cudaSetDevice(prev);
   delete h;
@@ -549,6 +579,115 @@ hgemm_status_t hgemm_run(hgemm_handle_t h, const void* A, const void* B, void* C
     args.tickets = h->tickets;
   }
   return cuda_status(dense_launch(kind, tmA, tmB, tmC, args, p.grid, s));
+}
+
+namespace {
+
+cudaError_t grow(void** p, size_t* cap, size_t need) {
+  if (*cap >= need) return cudaSuccess;
+  if (*p) {
+    cudaError_t e = cudaFree(*p);
+    *p = nullptr;
+    *cap = 0;
+    if (e != cudaSuccess) return e;
+  }
+  cudaError_t e = cudaMalloc(p, need);
+  if (e == cudaSuccess) *cap = need;
+  return e;
+}
+
+cudaError_t ensure_host_path(Ctx* c, Ctx::HostStage& st) {
+  cudaError_t e = cudaSuccess;
+  if (!c->s_h2d) e = cudaStreamCreateWithFlags(&c->s_h2d, cudaStreamNonBlocking);
+  if (e == cudaSuccess && !c->s_compute) e = cudaStreamCreateWithFlags(&c->s_compute, cudaStreamNonBlocking);
+  if (e == cudaSuccess && !c->s_d2h) e = cudaStreamCreateWithFlags(&c->s_d2h, cudaStreamNonBlocking);
+  if (e == cudaSuccess && !c->ev_entry) e = cudaEventCreateWithFlags(&c->ev_entry, cudaEventDisableTiming);
+  if (e == cudaSuccess && !c->ev_done) e = cudaEventCreateWithFlags(&c->ev_done, cudaEventDisableTiming);
+  if (e == cudaSuccess && !st.ev_free) e = cudaEventCreateWithFlags(&st.ev_free, cudaEventDisableTiming);
+  for (int i = 0; e == cudaSuccess && i < 8; ++i) {
+    if (!st.ev_a[i]) e = cudaEventCreateWithFlags(&st.ev_a[i], cudaEventDisableTiming);
+    if (e == cudaSuccess && !st.ev_c[i]) e = cudaEventCreateWithFlags(&st.ev_c[i], cudaEventDisableTiming);
+  }
+  return e;
+}
+
+}  // namespace
+
+hgemm_status_t hgemm_run_host(hgemm_handle_t h, const void* A, const void* B, void* C, int64_t M, int64_t N,
+                              int64_t K, hgemm_layout_t layout, hgemm_dtype_t in_dtype, hgemm_dtype_t acc_dtype,
+                              hgemm_dtype_t out_dtype, void* stream) {
+  if (!h) return HGEMM_ERR_INVALID_ARG;
+  hgemm_status_t st = check_problem(M, N, K, layout, in_dtype, acc_dtype, out_dtype);
+  if (st != HGEMM_OK) return st;
+  if (M == 0 || N == 0) return HGEMM_OK;
+  if (!C || (K > 0 && (!A || !B))) return HGEMM_ERR_INVALID_ARG;
+  const size_t a_bytes = (size_t)M * (size_t)K * 2, b_bytes = (size_t)K * (size_t)N * 2,
+               c_bytes = (size_t)M * (size_t)N * 2;
+  const uintptr_t a = reinterpret_cast<uintptr_t>(A), b = reinterpret_cast<uintptr_t>(B),
+                  c = reinterpret_cast<uintptr_t>(C);
+  if (overlaps(c, c_bytes, a, K > 0 ? a_bytes : 0) || overlaps(c, c_bytes, b, K > 0 ? b_bytes : 0))
+    return HGEMM_ERR_ALIAS;
+
+  Ctx::HostStage& sg = h->stage[h->stage_next];
+  cudaError_t e = ensure_host_path(h, sg);
+  if (e != cudaSuccess) return cuda_status(e);
+  // A set is reused two calls later: its previous copies out must be done
+  // before its buffers are reallocated or overwritten.
+  if (sg.used && (sg.a_cap < a_bytes || sg.b_cap < b_bytes || sg.c_cap < c_bytes)) {
+    e = cudaEventSynchronize(sg.ev_free);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  if ((e = grow(&sg.A, &sg.a_cap, a_bytes > 0 ? a_bytes : 16)) != cudaSuccess ||
+      (e = grow(&sg.B, &sg.b_cap, b_bytes > 0 ? b_bytes : 16)) != cudaSuccess ||
+      (e = grow(&sg.C, &sg.c_cap, c_bytes)) != cudaSuccess)
+    return e == cudaErrorMemoryAllocation ? HGEMM_ERR_OOM : cuda_status(e);
+
+  // Row chunks of A and C: at least 512 rows (whole 256-row tiles), at most 8.
+  int64_t rows = ((M + 7) / 8 + 255) / 256 * 256;
+  if (rows < 512) rows = 512;
+  const int nch = (int)((M + rows - 1) / rows);
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  char* Ad = static_cast<char*>(sg.A);
+  char* Cd = static_cast<char*>(sg.C);
+  const char* Ah = static_cast<const char*>(A);
+  char* Ch = static_cast<char*>(C);
+  // inputs go in after earlier work on the caller's stream and after the set is free
+  if ((e = cudaEventRecord(h->ev_entry, s)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(h->s_h2d, h->ev_entry, 0)) != cudaSuccess ||
+      (sg.used && (e = cudaStreamWaitEvent(h->s_h2d, sg.ev_free, 0)) != cudaSuccess))
+    return cuda_status(e);
+  if (K > 0 && (e = cudaMemcpyAsync(sg.B, B, b_bytes, cudaMemcpyHostToDevice, h->s_h2d)) != cudaSuccess)
+    return cuda_status(e);
+  for (int i = 0; i < nch; ++i) {
+    const int64_t r0 = i * rows, r1 = (r0 + rows < M) ? r0 + rows : M;
+    if (K > 0 && (e = cudaMemcpyAsync(Ad + r0 * K * 2, Ah + r0 * K * 2, (size_t)(r1 - r0) * K * 2,
+                                      cudaMemcpyHostToDevice, h->s_h2d)) != cudaSuccess)
+      return cuda_status(e);
+    if ((e = cudaEventRecord(sg.ev_a[i], h->s_h2d)) != cudaSuccess) return cuda_status(e);
+  }
+  for (int i = 0; i < nch; ++i) {
+    const int64_t r0 = i * rows, r1 = (r0 + rows < M) ? r0 + rows : M;
+    if ((e = cudaStreamWaitEvent(h->s_compute, sg.ev_a[i], 0)) != cudaSuccess) return cuda_status(e);
+    st = hgemm_run(h, K > 0 ? Ad + r0 * K * 2 : nullptr, K > 0 ? sg.B : nullptr, Cd + r0 * N * 2, r1 - r0, N, K,
+                   layout, in_dtype, acc_dtype, out_dtype, h->s_compute);
+    if (st != HGEMM_OK) return st;
+    if ((e = cudaEventRecord(sg.ev_c[i], h->s_compute)) != cudaSuccess) return cuda_status(e);
+  }
+  for (int i = 0; i < nch; ++i) {
+    const int64_t r0 = i * rows, r1 = (r0 + rows < M) ? r0 + rows : M;
+    if ((e = cudaStreamWaitEvent(h->s_d2h, sg.ev_c[i], 0)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(Ch + r0 * N * 2, Cd + r0 * N * 2, (size_t)(r1 - r0) * N * 2, cudaMemcpyDeviceToHost,
+                             h->s_d2h)) != cudaSuccess)
+      return cuda_status(e);
+  }
+  if ((e = cudaEventRecord(sg.ev_free, h->s_d2h)) != cudaSuccess ||
+      (e = cudaEventRecord(h->ev_done, h->s_d2h)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(s, h->ev_done, 0)) != cudaSuccess)
+    return cuda_status(e);
+  sg.used = true;
+  h->stage_next ^= 1;
+  return HGEMM_OK;
 }
 
 hgemm_status_t hgemm_trace_read(hgemm_handle_t h, hgemm_trace_record_t* out, int64_t capacity, int64_t* n_events) {

@@ -87,6 +87,8 @@ _lib.hgemm_destroy.restype = _i32
 _lib.hgemm_destroy.argtypes = [_vp]
 _lib.hgemm_run.restype = _i32
 _lib.hgemm_run.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _i32, _i32, _i32, _vp]
+_lib.hgemm_run_host.restype = _i32
+_lib.hgemm_run_host.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _i32, _i32, _i32, _vp]
 _lib.hgemm_sync_status.restype = _i32
 _lib.hgemm_sync_status.argtypes = [_vp, _vp, ctypes.POINTER(_i32)]
 _lib.hgemm_set_option.restype = _i32
@@ -166,6 +168,12 @@ def hgemm_destroy(h) -> int:
 def hgemm_run(h, A, B, C, M, N, K, layout, in_dtype, acc_dtype, out_dtype, stream=0) -> int:
     return int(_lib.hgemm_run(h, A, B, C, int(M), int(N), int(K), int(layout), int(in_dtype), int(acc_dtype),
                               int(out_dtype), stream))
+
+
+def hgemm_run_host(h, A, B, C, M, N, K, layout, in_dtype, acc_dtype, out_dtype, stream=0) -> int:
+    """End-to-end product on host buffers (see include/hgemm.h)."""
+    return int(_lib.hgemm_run_host(h, A, B, C, int(M), int(N), int(K), int(layout), int(in_dtype), int(acc_dtype),
+                                   int(out_dtype), stream))
 
 
 def hgemm_sync_status(h, stream=0):
@@ -286,6 +294,22 @@ class Handle:
         if check and st != HGEMM_OK:
             raise HgemmError(st, "hgemm_run")
         return st
+
+
+def _run_host_method(self, A, B, C, layout="TN", acc="f32", stream=None, check=True):
+    """C = A . B on CPU tensors (pinned for overlap); returns once enqueued."""
+    import torch
+    M, K = A.shape
+    N = B.shape[0] if layout == "TN" else B.shape[1]
+    s = stream if stream is not None else torch.cuda.current_stream()
+    st = hgemm_run_host(self.h, A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, LAYOUTS[layout],
+                        _torch_dtype(A.dtype), DTYPES[acc], _torch_dtype(C.dtype), s.cuda_stream)
+    if check and st != HGEMM_OK:
+        raise HgemmError(st, "hgemm_run_host")
+    return st
+
+
+Handle.run_host = _run_host_method
 
 
 def _torch_dtype(dt):

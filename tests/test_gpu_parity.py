@@ -259,3 +259,34 @@ def test_bounded_wait_gives_up_and_recovers(h, variant, M):
     # the context is still usable and the next launch is correct
     got = run(h, a, b, M, N, K, "TN", "f32", "bf16", variant)
     parity.check(got, ab, bb, M, N, K, "TN", "bf16", "f32", "bf16")
+
+
+@pytest.mark.parametrize("pinned", [True, False], ids=["pinned", "pageable"])
+@pytest.mark.parametrize("layout", ["TN", "NN"])
+@pytest.mark.parametrize("M,N,K", [(1000, 1000, 1024), (3000, 520, 200), (16, 2048, 4096), (5, 8, 0)])
+def test_run_host_end_to_end(h, M, N, K, layout, pinned):
+    a, b, ab, bb = parity.inputs(M, N, K, layout, "bf16", ("normal", 1.0), 81)
+    if pinned:
+        a, b = a.pin_memory(), b.pin_memory()
+    C = torch.full((M, N), float("nan"), dtype=torch.bfloat16)
+    if pinned:
+        C = C.pin_memory()
+    h.run_host(a, b, C, layout=layout, acc="f32")
+    st, detail = h.sync_status()
+    assert st == hgemm.HGEMM_OK, hex(detail)
+    parity.check(workloads.bits(C), ab, bb, M, N, K, layout, "bf16", "f32", "bf16")
+
+
+def test_run_host_back_to_back_calls(h):
+    # Consecutive calls alternate between two staging sets and overlap on the
+    # device; every output must still be the product of its own inputs.
+    M, N, K = 1536, 1024, 512
+    sets = [parity.inputs(M, N, K, "TN", "f16", ("uniform", -1.0, 1.0), 90 + i) for i in range(4)]
+    outs = []
+    for a, b, _, _ in sets:
+        C = torch.empty((M, N), dtype=torch.float16).pin_memory()
+        h.run_host(a.pin_memory(), b.pin_memory(), C, layout="TN", acc="f32")
+        outs.append(C)
+    assert h.sync_status()[0] == hgemm.HGEMM_OK
+    for (a, b, ab, bb), C in zip(sets, outs):
+        parity.check(workloads.bits(C), ab, bb, M, N, K, "TN", "f16", "f32", "f16")
