@@ -78,9 +78,11 @@ typedef enum {
 
 /* One intra-kernel trace event (HGEMM_OPT_TRACE).  t_ns is the GPU's global
  * nanosecond timer.  role: 0 CTA, 1 TMA producer, 2 MMA issuer, 3 epilogue.
- * kind: 1 kernel begin, 2 kernel end (after setup / before teardown), 3 item
+ * kind: 1 kernel begin, 2 kernel end (after setup / before teardown; value =
+ * the SM cycle counter's low 31 bits, so cycles / ns gives the clock), 3 item
  * begin, 4 item end, 5 stream-K partial stored (value = ticket drawn), 6 split
- * tile reduced (value = contributors).  item = tile index (-1 if none); value
+ * tile reduced (value = contributors), 7 cycles the role spent blocked on its
+ * barriers during the item (value).  item = tile index (-1 if none); value
  * for item begin/end = first / last k-block (epilogue: the stream-K slot). */
 typedef struct {
   uint64_t t_ns;
@@ -269,8 +271,8 @@ uint64_t hgemm_encode_smem_desc(uint32_t smem_addr, uint32_t lbo_bytes, uint32_t
  * or allocating library routine is called.
  *   A: device pointer, M x K row-major; B: device pointer, N x K row-major
  *   (TN); C: device pointer, M x N row-major, written.  The caller owns all three.
- *   Limits: 1 <= M <= 64 and N <= 33,554,432 (ceil(N/128) tickets fit in
- *   1 MiB); larger sizes return HGEMM_ERR_UNSUPPORTED.  M == 0 or N == 0 is a
+ *   Limits: 1 <= M <= 64 and N <= 33,554,432 (two counters for each of the
+ *   ceil(N/128) tiles fit in 2 MiB); larger sizes return HGEMM_ERR_UNSUPPORTED.  M == 0 or N == 0 is a
  *   no-op; K == 0 writes +0.  Alignment and aliasing rules are those of
  *   hgemm_run (HGEMM_ERR_MISALIGNED, HGEMM_ERR_ALIAS, HGEMM_ERR_INVALID_ARG).
  *   in_dtype, out_dtype: HGEMM_F16 or HGEMM_BF16.

@@ -513,7 +513,7 @@ hgemm_status_t hgemm_run(hgemm_handle_t h, const void* A, const void* B, void* C
         !encode_2d(&tmX, in_dtype, A, (uint64_t)K, (uint64_t)M, 64, (uint32_t)mma_n))
       return HGEMM_ERR_CUDA;
     const size_t partial_bytes = (size_t)p.grid * 2 * 128 * (size_t)mma_n * sizeof(float);
-    st = ensure_workspace(h, partial_bytes, (size_t)p.num_tiles, s);
+    st = ensure_workspace(h, partial_bytes, (size_t)p.num_tiles * 2, s);  // arrivals, publications
     if (st != HGEMM_OK) return st;
     if (p.smem_bytes > h->splitk_prepared_smem) return HGEMM_ERR_UNSUPPORTED;
     SplitKArgs args;

@@ -138,7 +138,7 @@ __global__ void __launch_bounds__(192, 1)
   pdl_launch_dependents();
   pdl_wait_prior_grid();
   TraceBuf* const tb = args.trace;
-  if (threadIdx.x == 0) trace_event(tb, 0, kTraceKernelBegin, -1, cluster);
+  if (threadIdx.x == 0) trace_event(tb, 0, kTraceKernelBegin, -1, (int32_t)(clock64() & 0x7fffffff));
 
   if (warp == 0) {
     // ------------------------------------------------- TMA producer ----
@@ -152,11 +152,12 @@ __global__ void __launch_bounds__(192, 1)
       WorkItem w;
       while (ok && it.next(w)) {
         trace_event(tb, kRoleProducer, kTraceItemBegin, w.tile, w.kb0);
+        uint32_t stall = 0;
         const TileCoord tc = tile_coord(w.tile, args.tiles_m, args.tiles_n, args.group_m);
         const int m_row = tc.m * (S::BM * CG) + (int)rank * S::BM;
         const int n_row = tc.n * BN + (int)rank * S::B_ROWS;
         for (int kb = w.kb0; kb < w.kb1; ++kb) {
-          if (!mbar_wait<kCS>(empty_bar(stage), phase ^ 1u, ctl)) {
+          if (!mbar_wait_stall<kCS>(empty_bar(stage), phase ^ 1u, ctl, &stall)) {
             ok = false;
             break;
           }
@@ -195,6 +196,7 @@ __global__ void __launch_bounds__(192, 1)
             phase ^= 1u;
           }
         }
+        trace_event(tb, kRoleProducer, kTraceStall, w.tile, (int32_t)stall);
         trace_event(tb, kRoleProducer, kTraceItemEnd, w.tile, w.kb1);
       }
       if (!ok) {
@@ -239,8 +241,9 @@ __global__ void __launch_bounds__(192, 1)
         tc_fence_after();
         trace_event(tb, kRoleMma, kTraceItemBegin, w.tile, w.kb0);
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        uint32_t stall = 0;
         for (int kb = w.kb0; kb < w.kb1; ++kb) {
-          if (!mbar_wait<kCS>(full_bar(stage), phase, ctl)) {
+          if (!mbar_wait_stall<kCS>(full_bar(stage), phase, ctl, &stall)) {
             ok = false;
             break;
           }
@@ -262,6 +265,7 @@ __global__ void __launch_bounds__(192, 1)
         }
         if (!ok) break;
         tc_commit_cg<CG>(tfull_bar(acc), (uint16_t)0x3);  // accumulator ready for the epilogue
+        trace_event(tb, kRoleMma, kTraceStall, w.tile, (int32_t)stall);
         trace_event(tb, kRoleMma, kTraceItemEnd, w.tile, w.kb1);
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
@@ -465,7 +469,7 @@ __global__ void __launch_bounds__(192, 1)
   }
 
   // --------------------------------------------------------- teardown ----
-  if (threadIdx.x == 0) trace_event(tb, 0, kTraceKernelEnd, -1, cluster);
+  if (threadIdx.x == 0) trace_event(tb, 0, kTraceKernelEnd, -1, (int32_t)(clock64() & 0x7fffffff));
   if constexpr (CG == 2) {
     // In a pair, the peer's loads signal CTA 0 and CTA 0's MMAs read the peer's
     // shared memory; after a give-up, leave time for copies still in flight.

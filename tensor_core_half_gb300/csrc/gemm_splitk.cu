@@ -55,7 +55,7 @@ int splitk_tmem_cols(int mma_n) { return sk_tmem_cols(mma_n); }
 size_t splitk_workspace_bytes(int grid, int mma_n, int n_tiles) {
   size_t partial = (size_t)grid * 2 * kRowsPerTile * (size_t)mma_n * sizeof(float);
   partial = (partial + 255) & ~(size_t)255;
-  return partial + (size_t)n_tiles * sizeof(int32_t);
+  return partial + (size_t)n_tiles * 2 * sizeof(int32_t);  // arrivals and publications
 }
 
 __device__ __forceinline__ void sk_report(int32_t* status, int32_t role, volatile uint32_t* abort_flag) {
@@ -149,7 +149,7 @@ __global__ void __launch_bounds__(192, 1)
   pdl_launch_dependents();
   pdl_wait_prior_grid();
   TraceBuf* const tb = args.trace;
-  if (threadIdx.x == 0) trace_event(tb, 0, kTraceKernelBegin, -1, (int32_t)begin);
+  if (threadIdx.x == 0) trace_event(tb, 0, kTraceKernelBegin, -1, (int32_t)(clock64() & 0x7fffffff));
 
   if (warp == 0) {
     // ---------------------------------------------------- TMA producer ----
@@ -290,37 +290,58 @@ __global__ void __launch_bounds__(192, 1)
             if (m < args.M) store_out(args.C, (int64_t)m * args.N + n, v[m], out_bf16);
         }
       } else {
-        // Publish our partial, then take a ticket; the last CTA of the tile reduces.
-        const int slot = sg.first ? 0 : 1;
-        float* mine = partials + (((int64_t)c * 2 + slot) * kRowsPerTile + row) * mma_n;
-#pragma unroll
-        for (int j = 0; j < kSplitKMaxM / 4; ++j)
-          if (j * 4 < mma_n) reinterpret_cast<float4*>(mine)[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-        named_bar_sync(1, 128);  // every row of our partial is written before the ticket
+        // Take a ticket first.  The last contributor keeps its own values in
+        // registers and adds the others' published partials to them; every other
+        // contributor publishes its partial and bumps the publication count.  The
+        // sum runs over the contributors in K order whoever arrives last.
         const int64_t u_first = (int64_t)sg.tile * args.k_blocks;
         const int64_t u_last = u_first + args.k_blocks - 1;
         const int64_t c_first = splitk_owner(u_first, args.units, G);
         const int64_t c_last = splitk_owner(u_last, args.units, G);
-        // acq_rel: publishes our partial and, for the last arriver, acquires the others'
-        if (threadIdx.x == 64) *ticket_slot = atom_add_acq_rel_gpu(args.tickets + sg.tile, 1);
+        const int32_t others = (int32_t)(c_last - c_first);
+        int32_t* const arrivals = args.tickets + sg.tile;
+        int32_t* const pubs = args.tickets + args.n_tiles + sg.tile;
+        if (threadIdx.x == 64) *ticket_slot = atomicAdd(arrivals, 1);
         named_bar_sync(1, 128);
         const int32_t ticket = *ticket_slot;
-        if (ticket == (int32_t)(c_last - c_first)) {
+        named_bar_sync(1, 128);
+        if (ticket != others) {
+          const int slot = sg.first ? 0 : 1;
+          float* mine = partials + (((int64_t)c * 2 + slot) * kRowsPerTile + row) * mma_n;
+#pragma unroll
+          for (int j = 0; j < kSplitKMaxM / 4; ++j)
+            if (j * 4 < mma_n)
+              reinterpret_cast<float4*>(mine)[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          named_bar_sync(1, 128);  // every row of the partial is written ...
+          if (threadIdx.x == 64) red_add_release_gpu(pubs, 1);  // ... before it is published
+        } else {
+          if (threadIdx.x == 64) {
+            const bool all_in = wait_counter_geq(pubs, others, ctl);
+            if (!all_in) sk_report(args.status, kRoleEpilogue, abort_flag);
+            *ticket_slot = all_in ? 1 : 0;
+          }
+          named_bar_sync(1, 128);  // the acquire above orders the partial reads below
+          const bool have_all = *ticket_slot != 0;
           float s[kSplitKMaxM];
 #pragma unroll
           for (int m = 0; m < kSplitKMaxM; ++m) s[m] = 0.0f;
           for (int64_t cc = c_first; cc <= c_last; ++cc) {
-            const int64_t cc_first_tile = splitk_begin(cc, args.units, G) / args.k_blocks;
-            const int cslot = (cc_first_tile == sg.tile) ? 0 : 1;
-            const float* src = partials + ((cc * 2 + cslot) * kRowsPerTile + row) * mma_n;
+            if (cc == c) {
 #pragma unroll
-            for (int j = 0; j < kSplitKMaxM / 4; ++j) {
-              if (j * 4 < mma_n) {
-                const float4 f = __ldcg(reinterpret_cast<const float4*>(src) + j);
-                if (cc == c_first) {
-                  s[4 * j] = f.x; s[4 * j + 1] = f.y; s[4 * j + 2] = f.z; s[4 * j + 3] = f.w;
-                } else {
-                  s[4 * j] += f.x; s[4 * j + 1] += f.y; s[4 * j + 2] += f.z; s[4 * j + 3] += f.w;
+              for (int m = 0; m < kSplitKMaxM; ++m) s[m] += v[m];
+            } else if (have_all) {
+              const int64_t cc_first_tile = splitk_begin(cc, args.units, G) / args.k_blocks;
+              const int cslot = (cc_first_tile == sg.tile) ? 0 : 1;
+              const float4* src =
+                  reinterpret_cast<const float4*>(partials + ((cc * 2 + cslot) * kRowsPerTile + row) * mma_n);
+#pragma unroll
+              for (int j = 0; j < kSplitKMaxM / 4; ++j) {
+                if (j * 4 < mma_n) {
+                  const float4 f = __ldcg(src + j);
+                  s[4 * j] += f.x;
+                  s[4 * j + 1] += f.y;
+                  s[4 * j + 2] += f.z;
+                  s[4 * j + 3] += f.w;
                 }
               }
             }
@@ -330,7 +351,10 @@ __global__ void __launch_bounds__(192, 1)
             for (int m = 0; m < kSplitKMaxM; ++m)
               if (m < args.M) store_out(args.C, (int64_t)m * args.N + n, s[m], out_bf16);
           }
-          if (threadIdx.x == 64) args.tickets[sg.tile] = 0;  // ready for the next launch
+          if (threadIdx.x == 64) {  // ready for the next launch
+            *arrivals = 0;
+            *pubs = 0;
+          }
         }
         named_bar_sync(1, 128);  // ticket_slot is reused by the next segment
       }
@@ -340,7 +364,7 @@ __global__ void __launch_bounds__(192, 1)
     if (!ok && lane == 0) sk_report(args.status, kRoleEpilogue, abort_flag);
   }
 
-  if (threadIdx.x == 0) trace_event(tb, 0, kTraceKernelEnd, -1, (int32_t)end);
+  if (threadIdx.x == 0) trace_event(tb, 0, kTraceKernelEnd, -1, (int32_t)(clock64() & 0x7fffffff));
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();

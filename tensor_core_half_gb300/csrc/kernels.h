@@ -22,12 +22,13 @@ struct TraceRecord {
   int32_t value;     // kind-specific (k-block range start, ticket, ...)
 };
 enum TraceKind : uint16_t {
-  kTraceKernelBegin = 1,    // after setup (value: cluster or first unit)
-  kTraceKernelEnd = 2,      // before teardown
+  kTraceKernelBegin = 1,    // after setup (value: SM clock counter, low 31 bits)
+  kTraceKernelEnd = 2,      // before teardown (value: SM clock counter, low 31 bits)
   kTraceItemBegin = 3,      // a role starts a work item (value: first k-block, or slot for the epilogue)
   kTraceItemEnd = 4,        // a role finishes it
   kTracePartialStored = 5,  // stream-K partial published (value: ticket drawn)
   kTraceReduced = 6,        // a split tile reduced and stored (value: contributors)
+  kTraceStall = 7,          // SM cycles the role spent blocked on barriers during the item
 };
 struct TraceBuf {
   unsigned long long count;  // records requested (may exceed capacity)
@@ -86,7 +87,7 @@ struct SplitKArgs {
   uint64_t timeout_ns;
   int32_t* status;
   float* partials;   // [grid][2][128][mma_n] fp32
-  int32_t* tickets;  // [n_tiles], all zero between launches
+  int32_t* tickets;  // [2][n_tiles] arrivals, publications; all zero between launches
   void* C;           // [M][N] row-major
   TraceBuf* trace;   // null unless tracing
 };

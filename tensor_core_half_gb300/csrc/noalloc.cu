@@ -29,7 +29,7 @@ namespace {
 // Scratch layout: [status word | per-tile tickets | fp32 partial sums].
 constexpr size_t kNoAllocScratchBytes = (size_t)16 << 20;  // 16 MiB
 constexpr size_t kStatusBytes = 256;
-constexpr size_t kTicketBytes = (size_t)1 << 20;  // 262144 tickets: N <= 33,554,432
+constexpr size_t kTicketBytes = (size_t)2 << 20;  // 2 counters x 262144 tiles: N <= 33,554,432
 constexpr size_t kPartialOffset = kStatusBytes + kTicketBytes;
 constexpr size_t kPartialBytes = kNoAllocScratchBytes - kPartialOffset;
 constexpr int kMaxDevices = 64;
@@ -121,7 +121,7 @@ extern "C" hgemm_status_t hgemm_run_splitk_noalloc(const void* A, const void* B,
   if (M == 0 || N == 0) return HGEMM_OK;
   if (M > hg::kSplitKMaxM) return HGEMM_ERR_UNSUPPORTED;  // beyond the scratch layout's maximum
   const int64_t n_tiles = (N + 127) / 128;
-  if ((size_t)n_tiles * sizeof(int32_t) > kTicketBytes) return HGEMM_ERR_UNSUPPORTED;
+  if ((size_t)n_tiles * 2 * sizeof(int32_t) > kTicketBytes) return HGEMM_ERR_UNSUPPORTED;
   if (N % 8 != 0 || (K > 0 && K % 8 != 0)) return HGEMM_ERR_MISALIGNED;
   if (!C || (K > 0 && (!A || !B))) return HGEMM_ERR_INVALID_ARG;
   const uintptr_t a = reinterpret_cast<uintptr_t>(A), b = reinterpret_cast<uintptr_t>(B),
@@ -161,7 +161,7 @@ extern "C" hgemm_status_t hgemm_run_splitk_noalloc(const void* A, const void* B,
 
   // The array keeps whatever the previous call left: clear the status word and
   // the tickets this call uses (they must start at zero), on the same stream.
-  const size_t clear = (kStatusBytes + (size_t)n_tiles * sizeof(int32_t) + 15) & ~(size_t)15;
+  const size_t clear = (kStatusBytes + (size_t)n_tiles * 2 * sizeof(int32_t) + 15) & ~(size_t)15;
   if (hg::fill_zero_launch(d->scratch, clear, s) != cudaSuccess) return HGEMM_ERR_CUDA;
 
   hg::SplitKArgs args;

@@ -179,6 +179,17 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
   return mbar_wait_slow<kClusterScope>(bar, parity, ctl);
 }
 
+// Same as mbar_wait, adding the SM cycles spent blocked (slow path only) to *stall.
+template <bool kClusterScope = false>
+__device__ __forceinline__ bool mbar_wait_stall(uint32_t bar, uint32_t parity, const WaitCtl& ctl, uint32_t* stall) {
+  bool ok = kClusterScope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+  if (ok) return true;
+  const long long c0 = clock64();
+  ok = mbar_wait_slow<kClusterScope>(bar, parity, ctl);
+  *stall += (uint32_t)(clock64() - c0);
+  return ok;
+}
+
 // -------------------------------------------------------------------- TMA ----
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");

@@ -12,7 +12,8 @@ import collections
 import json
 
 ROLES = {0: "cta", 1: "tma", 2: "mma", 3: "epilogue"}
-KINDS = {1: "kernel_begin", 2: "kernel_end", 3: "item_begin", 4: "item_end", 5: "partial_stored", 6: "reduced"}
+KINDS = {1: "kernel_begin", 2: "kernel_end", 3: "item_begin", 4: "item_end", 5: "partial_stored", 6: "reduced",
+         7: "stall_cycles"}
 
 
 def spans(rows):
@@ -46,7 +47,20 @@ def summary(rows):
     for s in sp:
         busy[s["role"]] += s["t1"] - s["t0"]
     n_cta = max(1, len(begins))
+    # SM clock: cycle-counter delta over timer delta between a CTA's begin and end
+    be = {}
+    for t, cta, role, kind, item, value in rows:
+        if kind in (1, 2):
+            be.setdefault(cta, {})[kind] = (t, value)
+    mhz = [((v[2][1] - v[1][1]) % (1 << 31)) / max(1, v[2][0] - v[1][0]) * 1e3
+           for v in be.values() if 1 in v and 2 in v and v[2][0] > v[1][0]]
+    stalls = collections.defaultdict(int)
+    for r in rows:
+        if r[3] == 7:
+            stalls[ROLES.get(r[2], str(r[2]))] += r[5]
     return {
+        "sm_mhz": sorted(mhz)[len(mhz) // 2] if mhz else None,
+        "stall_cycles_per_cta": {k: v / n_cta for k, v in stalls.items()},
         "span_ns": max(r[0] for r in rows) - t0,
         "cta_begin_ns": [min(begins), max(begins)] if begins else None,
         "cta_end_ns": [min(ends), max(ends)] if ends else None,
