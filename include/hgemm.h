@@ -59,7 +59,8 @@ typedef enum {
   HGEMM_VARIANT_1SM_128x128 = 1, /* persistent tcgen05, one CTA per 128x128 C tile          */
   HGEMM_VARIANT_1SM_128x256 = 2, /* persistent tcgen05, one CTA per 128x256 C tile          */
   HGEMM_VARIANT_2SM_256x256 = 3, /* persistent tcgen05 cta_group::2, a CTA pair per 256x256 */
-  HGEMM_VARIANT_SPLITK = 4       /* skinny M (TN, fp32 accumulate, M <= 64): swap-AB split-K */
+  HGEMM_VARIANT_SPLITK = 4,      /* skinny M (TN, fp32 accumulate, M <= 64): swap-AB split-K */
+  HGEMM_VARIANT_2SM_256x192 = 5  /* as 2SM_256x256 with 192-column tiles (TN only)            */
 } hgemm_variant_t;
 
 /* Handle options (hgemm_set_option). */

@@ -64,7 +64,7 @@ struct Ctx {
   int stage_next = 0;
   cudaStream_t s_h2d = nullptr, s_compute = nullptr, s_d2h = nullptr;
   cudaEvent_t ev_entry = nullptr, ev_done = nullptr;
-  int capacity[3] = {0, 0, 0};  // resident clusters per dense kind
+  int capacity[kNumDenseKinds] = {};  // resident clusters per dense kind
   int splitk_prepared_smem = 0;
 };
 
@@ -101,6 +101,7 @@ DenseKind kind_of(int variant) {
   switch (variant) {
     case HGEMM_VARIANT_1SM_128x128: return kDense1Sm128;
     case HGEMM_VARIANT_1SM_128x256: return kDense1Sm256;
+    case HGEMM_VARIANT_2SM_256x192: return kDense2Sm192;
     default: return kDense2Sm256;
   }
 }
@@ -109,6 +110,7 @@ int variant_of(DenseKind k) {
   switch (k) {
     case kDense1Sm128: return HGEMM_VARIANT_1SM_128x128;
     case kDense1Sm256: return HGEMM_VARIANT_1SM_128x256;
+    case kDense2Sm192: return HGEMM_VARIANT_2SM_256x192;
     default: return HGEMM_VARIANT_2SM_256x256;
   }
 }
@@ -144,7 +146,8 @@ DenseChoice dense_choice(DenseKind kind, int64_t M, int64_t N, int64_t K, int ca
     sk.cost = (double)tiles / (double)sk.clusters + 30.0 / (double)kb;
     if (sk.cost < dp.cost) best = sk;
   }
-  const double eff = (kind == kDense2Sm256) ? 1.0 : (kind == kDense1Sm256 ? 0.85 : 0.70);
+  // relative mainloop efficiency per tile area (2-SM 256-wide tiles are the reference)
+  const double eff = (kind == kDense2Sm256) ? 1.0 : (kind == kDense2Sm192 ? 0.78 : (kind == kDense1Sm256 ? 0.85 : 0.70));
   best.cost *= (double)(128 * info.cta_group) * (double)info.block_n / (double)info.cta_group / eff;
   return best;
 }
@@ -176,15 +179,15 @@ void fill_dense_plan(DenseKind kind, const DenseChoice& ch, int64_t M, int64_t N
 }
 
 hgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int layout, int in, int acc, int out, int num_sms,
-                         int smem_optin, const int capacity_in[3], int variant, int group_m, int max_ctas,
+                         int smem_optin, const int capacity_in[kNumDenseKinds], int variant, int group_m, int max_ctas,
                          bool allow_sk, hgemm_plan_t* p) {
   memset(p, 0, sizeof(*p));
   hgemm_status_t st = check_problem(M, N, K, layout, in, acc, out);
   if (st != HGEMM_OK) return st;
   if (num_sms <= 0) return HGEMM_ERR_INVALID_ARG;
-  if (variant < HGEMM_VARIANT_AUTO || variant > HGEMM_VARIANT_SPLITK) return HGEMM_ERR_INVALID_ARG;
-  int capacity[3];
-  for (int i = 0; i < 3; ++i) {
+  if (variant < HGEMM_VARIANT_AUTO || variant > HGEMM_VARIANT_2SM_256x192) return HGEMM_ERR_INVALID_ARG;
+  int capacity[kNumDenseKinds];
+  for (int i = 0; i < kNumDenseKinds; ++i) {
     const DenseKindInfo info = dense_kind_info((DenseKind)i);
     capacity[i] = (capacity_in && capacity_in[i] > 0) ? capacity_in[i] : num_sms / info.cta_group;
   }
@@ -222,10 +225,12 @@ hgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int layout, int in, in
   DenseChoice choice{};
   if (variant != HGEMM_VARIANT_AUTO) {
     kind = kind_of(variant);
+    if (layout == HGEMM_LAYOUT_NN && !dense_kind_allows_nn(kind)) return HGEMM_ERR_UNSUPPORTED;
     choice = dense_choice(kind, M, N, K, capacity[kind], max_ctas, allow_sk);
   } else {
     bool first = true;
-    for (DenseKind k : {kDense2Sm256, kDense1Sm256, kDense1Sm128}) {
+    for (DenseKind k : {kDense2Sm256, kDense2Sm192, kDense1Sm256, kDense1Sm128}) {
+      if (layout == HGEMM_LAYOUT_NN && !dense_kind_allows_nn(k)) continue;
       const DenseChoice c = dense_choice(k, M, N, K, capacity[k], max_ctas, allow_sk);
       if (first || c.cost < choice.cost) {
         choice = c;
@@ -387,7 +392,7 @@ hgemm_status_t hgemm_create(hgemm_handle_t* out) {
   }
   e = cudaMalloc(&c->status, 16);
   if (e == cudaSuccess) e = cudaMemset(c->status, 0, 16);
-  for (int k = 0; e == cudaSuccess && k < 3; ++k) {
+  for (int k = 0; e == cudaSuccess && k < kNumDenseKinds; ++k) {
     e = dense_prepare((DenseKind)k);
     if (e == cudaSuccess) e = dense_max_active_clusters((DenseKind)k, &c->capacity[k]);
   }
@@ -438,7 +443,7 @@ hgemm_status_t hgemm_set_option(hgemm_handle_t h, int32_t option, int64_t value)
   if (!h) return HGEMM_ERR_INVALID_ARG;
   switch (option) {
     case HGEMM_OPT_FORCE_VARIANT:
-      if (value < HGEMM_VARIANT_AUTO || value > HGEMM_VARIANT_SPLITK) return HGEMM_ERR_INVALID_ARG;
+      if (value < HGEMM_VARIANT_AUTO || value > HGEMM_VARIANT_2SM_256x192) return HGEMM_ERR_INVALID_ARG;
       h->force_variant = (int)value;
       return HGEMM_OK;
     case HGEMM_OPT_TIMEOUT_NS:

@@ -50,10 +50,12 @@ struct DenseShape {
   static constexpr int NUM_BARS = 2 * STAGES + 5;  // full[S], empty[S], tmem_full[2], tmem_empty[2], drain
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + alignment slack for the 1 KiB base
-  static constexpr int TMEM_COLS = 2 * BN;
+  static constexpr int TMEM_COLS = 2 * BN <= 256 ? 256 : 512;  // two accumulators, power of two
   static constexpr int THREADS = 192;
   static_assert(BN % 64 == 0 && BN <= 256, "BN");
-  static_assert((BN / CG) % 64 == 0, "B slice must be whole 64-column boxes");
+  static_assert((BN / CG) % 8 == 0, "B slice rows");
+  // An MN-major (NN) B slice is loaded as 64-column boxes.
+  static constexpr bool kMNMajorOK = (BN / CG) % 64 == 0;
   static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation must be a power of two");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
@@ -172,7 +174,7 @@ __global__ void __launch_bounds__(192, 1)
               tma_load_2d(a_dst, &tmA, fb, k0, m_row);
               if (!args.b_mn_major) {
                 tma_load_2d(b_dst, &tmB, fb, k0, n_row);
-              } else {
+              } else if constexpr (S::kMNMajorOK) {
 #pragma unroll
                 for (int j = 0; j < S::B_ROWS / 64; ++j) tma_load_2d(b_dst + j * 8192, &tmB, fb, n_row + 64 * j, k0);
               }
@@ -183,7 +185,7 @@ __global__ void __launch_bounds__(192, 1)
               tma_load_2d_pair(a_dst, &tmA, fb, k0, m_row);
               if (!args.b_mn_major) {
                 tma_load_2d_pair(b_dst, &tmB, fb, k0, n_row);
-              } else {
+              } else if constexpr (S::kMNMajorOK) {
 #pragma unroll
                 for (int j = 0; j < S::B_ROWS / 64; ++j)
                   tma_load_2d_pair(b_dst + j * 8192, &tmB, fb, n_row + 64 * j, k0);
@@ -492,7 +494,8 @@ __global__ void __launch_bounds__(192, 1)
 #define HG_DENSE_KINDS(X) \
   X(kDense1Sm128, 1, 128, 6) \
   X(kDense1Sm256, 1, 256, 4) \
-  X(kDense2Sm256, 2, 256, 6)
+  X(kDense2Sm256, 2, 256, 6) \
+  X(kDense2Sm192, 2, 192, 6)
 
 DenseKindInfo dense_kind_info(DenseKind kind) {
   switch (kind) {

@@ -59,7 +59,10 @@ struct DenseArgs {
   TraceBuf* trace;         // null unless tracing
 };
 
-enum DenseKind : int { kDense1Sm128 = 0, kDense1Sm256 = 1, kDense2Sm256 = 2 };
+enum DenseKind : int { kDense1Sm128 = 0, kDense1Sm256 = 1, kDense2Sm256 = 2, kDense2Sm192 = 3 };
+constexpr int kNumDenseKinds = 4;
+// Kinds whose B slice per CTA is a whole number of 64-column boxes (NN layout).
+inline bool dense_kind_allows_nn(DenseKind k) { return k != kDense2Sm192; }
 
 struct DenseKindInfo {
   int cta_group, block_n, stages, smem_bytes, tmem_cols, threads;

@@ -49,6 +49,7 @@ HGEMM_VARIANT_1SM_128x128 = 1
 HGEMM_VARIANT_1SM_128x256 = 2
 HGEMM_VARIANT_2SM_256x256 = 3
 HGEMM_VARIANT_SPLITK = 4
+HGEMM_VARIANT_2SM_256x192 = 5
 
 HGEMM_OPT_FORCE_VARIANT = 1
 HGEMM_OPT_TIMEOUT_NS = 2
@@ -61,7 +62,7 @@ HGEMM_OPT_TRACE = 7
 LAYOUTS = {"TN": HGEMM_LAYOUT_TN, "NN": HGEMM_LAYOUT_NN}
 DTYPES = {"f16": HGEMM_F16, "bf16": HGEMM_BF16, "f32": HGEMM_F32}
 VARIANTS = {"auto": HGEMM_VARIANT_AUTO, "1sm128": HGEMM_VARIANT_1SM_128x128, "1sm256": HGEMM_VARIANT_1SM_128x256,
-            "2sm256": HGEMM_VARIANT_2SM_256x256, "splitk": HGEMM_VARIANT_SPLITK}
+            "2sm256": HGEMM_VARIANT_2SM_256x256, "splitk": HGEMM_VARIANT_SPLITK, "2sm192": HGEMM_VARIANT_2SM_256x192}
 
 
 class hgemm_plan_t(ctypes.Structure):

@@ -63,6 +63,7 @@ def test_plan_dtype_and_layout_validation():
     assert plan(64, 64, 64, fin=H.HGEMM_F16, acc=H.HGEMM_F16, out=H.HGEMM_F16)[0] == ST_OK
     assert plan(64, 64, 64, sms=0)[0] == ST_INV
     assert plan(64, 64, 64, variant=9)[0] == ST_INV
+    assert plan(64, 64, 64, variant=6)[0] == ST_INV
 
 
 def test_plan_variant_choice():
@@ -72,7 +73,7 @@ def test_plan_variant_choice():
     assert p.grid == 152 and p.tmem_cols == 512 and p.smem_bytes <= 232448
     # 256 tiles over 76 pairs: two whole waves data-parallel, the rest stream-K
     assert p.stream_k == 1 and p.dp_tiles == 152 and p.sk_units == (256 - 152) * 64
-    st, p = plan(4096, 4096, 4096, stream_k=0)
+    st, p = plan(4096, 4096, 4096, stream_k=0, variant=3)
     assert st == ST_OK and p.stream_k == 0 and p.dp_tiles == 256 and p.sk_units == 0 and p.workspace_bytes == 0
     # a tile count that is a whole number of waves stays data-parallel
     st, p = plan(256 * 76, 256, 4096)
@@ -86,9 +87,15 @@ def test_plan_variant_choice():
     assert st == ST_OK and p.variant != H.HGEMM_VARIANT_SPLITK  # and fp32 accumulate only
     assert plan(16, 64, 64, layout=1, variant=H.HGEMM_VARIANT_SPLITK)[0] == ST_UNS
     assert plan(65, 64, 64, variant=H.HGEMM_VARIANT_SPLITK)[0] == ST_UNS
-    for v in (1, 2, 3):
+    for v in (1, 2, 3, 5):
         st, p = plan(1000, 3000, 4104, variant=v)
         assert st == ST_OK and p.variant == v
+    # the ragged shape: 256 x 192 tiles give 64 tiles (one wave, no stream-K fix-ups)
+    st, p = plan(1000, 3000, 4104)
+    assert st == ST_OK and p.variant == H.HGEMM_VARIANT_2SM_256x192 and p.num_tiles == 64 and p.stream_k == 0
+    assert plan(1000, 3000, 4104, layout=H.HGEMM_LAYOUT_NN, variant=5)[0] == ST_UNS
+    st, p = plan(1000, 3000, 4104, layout=H.HGEMM_LAYOUT_NN)
+    assert st == ST_OK and p.variant != H.HGEMM_VARIANT_2SM_256x192
     st, p = plan(1000, 3000, 4104, variant=1)
     assert (p.tiles_m, p.tiles_n, p.k_blocks) == (8, 24, 65)
 
@@ -170,6 +177,7 @@ def test_shared_memory_descriptor_bits(args, word):
 
 
 STREAMK_CASES = [(4096, 4096, 4096, 3), (2048, 2048, 2048, 3), (1000, 3000, 4104, 1), (1000, 3000, 4104, 3),
+                 (4096, 4096, 4096, 5), (3000, 6000, 2048, 5),
                  (8192, 8192, 8192, 3), (256, 256, 4096, 3), (640, 1024, 2048, 2), (256, 512, 128, 3)]
 
 
