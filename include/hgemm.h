@@ -73,9 +73,26 @@ typedef enum {
   HGEMM_OPT_MAX_CTAS = 5,      /* value: cap on persistent CTAs (0 = one per SM)              */
   HGEMM_OPT_STREAM_K = 6,      /* value: 1 (default) lets the planner split the last wave of
                                   dense tiles along K (stream-K); 0 keeps every tile whole    */
-  HGEMM_OPT_TRACE = 7          /* value: capacity in events of a device trace buffer that the
+  HGEMM_OPT_TRACE = 7,         /* value: capacity in events of a device trace buffer that the
                                   kernels append to (0 = off, the default); hgemm_trace_read */
+  HGEMM_OPT_SCHEDULE = 8       /* value: an hgemm_schedule_t for the dense kernels           */
 } hgemm_option_t;
+
+/*
+ * Dense work schedules (HGEMM_OPT_SCHEDULE).  Both cut the same work into
+ * the same work ids (hgemm_plan_t: sk_ranges stream-K ranges, then dp_tiles
+ * whole tiles) and give bitwise identical results.
+ *   STATIC (default): plan->grid / cta_group persistent clusters; cluster c
+ *     takes ids c, c + P, c + 2P, ... (P clusters).
+ *   DYNAMIC: plan->work_ids clusters are launched, one per id; a cluster that
+ *     finishes an id cancels the launch of a cluster that has not started
+ *     (Blackwell cluster launch control) and takes over its id, so the ids
+ *     spread over the clusters that actually run (other work on the GPU,
+ *     uneven SM speed).  The "Persistent kernel" section of "tcgen05 for
+ *     dummies: a B200 GEMM from scratch" names this as the step after static
+ *     scheduling.
+ */
+typedef enum { HGEMM_SCHEDULE_STATIC = 0, HGEMM_SCHEDULE_DYNAMIC = 1 } hgemm_schedule_t;
 
 /* One intra-kernel trace event (HGEMM_OPT_TRACE).  t_ns is the GPU's global
  * nanosecond timer.  role: 0 CTA, 1 TMA producer, 2 MMA issuer, 3 epilogue.
@@ -200,6 +217,8 @@ typedef struct {
   int32_t dp_tiles;      /* dense: tiles computed whole, dealt round-robin (all if no stream-K) */
   int32_t stream_k;      /* dense: 1 when the remaining tiles are split along K            */
   int64_t sk_units;      /* dense: (num_tiles - dp_tiles) * k_blocks, cut evenly over clusters */
+  int32_t sk_ranges;     /* dense: stream-K ranges, work ids [0, sk_ranges); 0 without stream-K */
+  int32_t work_ids;      /* dense: sk_ranges + dp_tiles; ids >= sk_ranges are whole tiles  */
 } hgemm_plan_t;
 
 /*
@@ -222,6 +241,15 @@ hgemm_status_t hgemm_plan(int64_t M, int64_t N, int64_t K, hgemm_layout_t layout
  */
 hgemm_status_t hgemm_plan_work_item(const hgemm_plan_t* plan, int32_t cluster, int32_t index, int32_t* tile,
                                     int32_t* kb0, int32_t* kb1, int32_t* slot);
+
+/*
+ * hgemm_plan_id_item -- the index-th item of work id `id` (0 <= id <
+ * plan->work_ids) of a dense plan, in the same form as hgemm_plan_work_item.
+ * Under HGEMM_SCHEDULE_DYNAMIC a cluster runs whole ids in whatever order
+ * cluster launch control hands them out.  INVALID_ARG past the id's end.
+ */
+hgemm_status_t hgemm_plan_id_item(const hgemm_plan_t* plan, int32_t id, int32_t index, int32_t* tile, int32_t* kb0,
+                                  int32_t* kb1, int32_t* slot);
 
 /*
  * hgemm_plan_tile -- the persistent scheduler's map from a linear tile index

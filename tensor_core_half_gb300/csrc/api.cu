@@ -47,6 +47,7 @@ struct Ctx {
   int group_m = kDefaultGroupM;
   int max_ctas = 0;
   bool stream_k = true;
+  int schedule = HGEMM_SCHEDULE_STATIC;
   TraceBuf* trace = nullptr;  // device trace buffer (HGEMM_OPT_TRACE)
   int64_t trace_capacity = 0;
   // hgemm_run_host: two staging sets (double buffering across calls), three
@@ -172,6 +173,8 @@ void fill_dense_plan(DenseKind kind, const DenseChoice& ch, int64_t M, int64_t N
   p->dp_tiles = ch.dp_tiles;
   p->sk_units = ch.sk_units;
   p->stream_k = ch.sk_units > 0 ? 1 : 0;
+  p->sk_ranges = p->stream_k ? ch.clusters : 0;
+  p->work_ids = p->sk_ranges + ch.dp_tiles;
   p->workspace_bytes =
       p->stream_k ? (int64_t)ch.clusters * 2 * info.cta_group * info.block_n * 128 * 4 +
                         (int64_t)p->num_tiles * info.cta_group * 8
@@ -340,10 +343,28 @@ hgemm_status_t hgemm_plan_work_item(const hgemm_plan_t* plan, int32_t cluster, i
     return HGEMM_ERR_INVALID_ARG;
   const int32_t nclusters = plan->grid / plan->cta_group;
   if (cluster < 0 || cluster >= nclusters) return HGEMM_ERR_INVALID_ARG;
-  WorkIter it(cluster, nclusters, plan->dp_tiles, plan->sk_units, plan->k_blocks);
+  WorkIter it(plan->sk_ranges, plan->dp_tiles, plan->sk_units, plan->k_blocks);
+  it.start_static(cluster, nclusters);
   WorkItem w;
   for (int32_t i = 0; i <= index; ++i)
-    if (!it.next(w)) return HGEMM_ERR_INVALID_ARG;
+    if (!it.next_static(w)) return HGEMM_ERR_INVALID_ARG;
+  *tile = w.tile;
+  *kb0 = w.kb0;
+  *kb1 = w.kb1;
+  *slot = w.slot;
+  return HGEMM_OK;
+}
+
+hgemm_status_t hgemm_plan_id_item(const hgemm_plan_t* plan, int32_t id, int32_t index, int32_t* tile, int32_t* kb0,
+                                  int32_t* kb1, int32_t* slot) {
+  if (!plan || !tile || !kb0 || !kb1 || !slot || plan->variant == HGEMM_VARIANT_SPLITK || plan->cta_group < 1 ||
+      index < 0 || id < 0 || id >= plan->work_ids)
+    return HGEMM_ERR_INVALID_ARG;
+  WorkIter it(plan->sk_ranges, plan->dp_tiles, plan->sk_units, plan->k_blocks);
+  it.start(id);
+  WorkItem w;
+  for (int32_t i = 0; i <= index; ++i)
+    if (!it.next_in_id(w)) return HGEMM_ERR_INVALID_ARG;
   *tile = w.tile;
   *kb0 = w.kb0;
   *kb1 = w.kb1;
@@ -466,6 +487,10 @@ hgemm_status_t hgemm_set_option(hgemm_handle_t h, int32_t option, int64_t value)
       if (value < 0 || value > 1) return HGEMM_ERR_INVALID_ARG;
       h->stream_k = value != 0;
       return HGEMM_OK;
+    case HGEMM_OPT_SCHEDULE:
+      if (value != HGEMM_SCHEDULE_STATIC && value != HGEMM_SCHEDULE_DYNAMIC) return HGEMM_ERR_INVALID_ARG;
+      h->schedule = (int)value;
+      return HGEMM_OK;
     case HGEMM_OPT_TRACE: {
       if (value < 0 || value > (int64_t)1 << 26) return HGEMM_ERR_INVALID_ARG;
       if (h->trace) {
@@ -571,7 +596,9 @@ hgemm_status_t hgemm_run(hgemm_handle_t h, const void* A, const void* B, void* C
   args.status = h->status;
   args.trace = h->trace;
   args.dp_tiles = p.dp_tiles;
+  args.sk_ranges = p.sk_ranges;
   args.sk_units = p.sk_units;
+  args.dynamic = h->schedule == HGEMM_SCHEDULE_DYNAMIC ? 1 : 0;
   args.partials = nullptr;
   args.tickets = nullptr;
   if (p.stream_k) {
@@ -583,7 +610,10 @@ hgemm_status_t hgemm_run(hgemm_handle_t h, const void* A, const void* B, void* C
     args.partials = h->partials;
     args.tickets = h->tickets;
   }
-  return cuda_status(dense_launch(kind, tmA, tmB, tmC, args, p.grid, s));
+  // Dynamic schedule: one cluster per work id; the clusters that run first
+  // take over the ids of those that have not started.
+  const int grid = args.dynamic ? p.work_ids * info.cta_group : p.grid;
+  return cuda_status(dense_launch(kind, tmA, tmB, tmC, args, grid, s));
 }
 
 namespace {

@@ -47,9 +47,12 @@ struct DenseShape {
   static constexpr int EPI_BYTES = 4 * 2 * EPI_BOX_BYTES;  // 4 warps x double buffer
   static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
   static constexpr int BAR_OFF = RING_BYTES + EPI_BYTES;
-  static constexpr int NUM_BARS = 2 * STAGES + 5;  // full[S], empty[S], tmem_full[2], tmem_empty[2], drain
+  static constexpr int CLC_SLOTS = 4;             // cluster-launch-control responses in flight
+  // full[S], empty[S], tmem_full[2], tmem_empty[2], drain, clc_full[C], clc_empty[C]
+  static constexpr int NUM_BARS = 2 * STAGES + 5 + 2 * CLC_SLOTS;
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
-  static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + alignment slack for the 1 KiB base
+  static constexpr int CLC_OFF = (MISC_OFF + 16 + 15) / 16 * 16;  // 16-byte responses
+  static constexpr int SMEM_BYTES = CLC_OFF + 16 * CLC_SLOTS + 1024;  // + alignment slack for the 1 KiB base
   static constexpr int TMEM_COLS = 2 * BN <= 256 ? 256 : 512;  // two accumulators, power of two
   static constexpr int THREADS = 192;
   static_assert(BN % 64 == 0 && BN <= 256, "BN");
@@ -73,6 +76,97 @@ __device__ __forceinline__ uint32_t f16x2_to_out(uint32_t h2, bool out_bf16) {
   return pack_f32x2_to_bf16x2(f.x, f.y);
 }
 
+// The work ids one role walks through.  Static schedule: the cluster's fixed
+// walk.  Dynamic schedule: the cluster's own id, then ids taken over from
+// clusters that have not started, by cluster launch control ("Persistent
+// kernel" section of the tcgen05 walkthrough: the page names dynamic
+// scheduling as the next step after its static scheduler).  One thread of the
+// pair (the issuer) asks for the next id as soon as it starts an id; every
+// role reads each response from its own shared memory and then arrives on
+// the slot's empty barrier in CTA 0, so the slot can take the next request.
+template <int CG, int SLOTS>
+struct IdFeed {
+  WorkIter it;
+  int32_t cluster, nclusters;
+  bool dynamic, issuer, warp_wide, arrive;
+  bool started = false, finished = false;
+  int32_t taken = 0;      // responses read
+  int32_t requested = 0;  // requests issued (issuer only)
+  uint32_t resp0, full0, empty0;  // slot 0 addresses in this CTA
+
+  __device__ IdFeed(const DenseArgs& a, int32_t cluster_, int32_t nclusters_, uint32_t resp0_, uint32_t full0_,
+                    uint32_t empty0_, bool issuer_, bool warp_wide_, bool arrive_)
+      : it(a.sk_ranges, a.dp_tiles, a.sk_units, a.k_blocks),
+        cluster(cluster_),
+        nclusters(nclusters_),
+        dynamic(a.dynamic != 0),
+        issuer(issuer_),
+        warp_wide(warp_wide_),
+        arrive(arrive_),
+        resp0(resp0_),
+        full0(full0_),
+        empty0(empty0_) {}
+
+  __device__ bool request(const WaitCtl& ctl) {
+    const int32_t r = requested;  // 0-based request number
+    const uint32_t slot = (uint32_t)(r % SLOTS);
+    if (!mbar_wait<CG == 2>(empty0 + 8u * slot, (uint32_t)(((r / SLOTS) & 1) ^ 1), ctl)) return false;
+    const uint32_t fb = full0 + 8u * slot;
+    mbar_arrive_expect_tx(fb, 16);
+    if constexpr (CG == 2) mbar_arrive_expect_tx_cluster(mapa_shared(fb, 1), 16);
+    clc_try_cancel<CG>(resp0 + 16u * slot, fb);
+    ++requested;
+    return true;
+  }
+
+  // 1: an item in w; 0: no work left; -1: a wait gave up.
+  __device__ int next(WorkItem& w, const WaitCtl& ctl) {
+    for (;;) {
+      if (!started) {
+        if (finished) return 0;
+        started = true;
+        if (!dynamic) {
+          it.start_static(cluster, nclusters);
+        } else {
+          it.start(cluster);
+          if (issuer && !request(ctl)) return -1;
+        }
+      }
+      if (!dynamic) return it.next_static(w) ? 1 : 0;
+      if (it.next_in_id(w)) return 1;
+      const int32_t r = taken;  // 0-based response number
+      const uint32_t slot = (uint32_t)(r % SLOTS);
+      if (!mbar_wait<CG == 2>(full0 + 8u * slot, (uint32_t)((r / SLOTS) & 1), ctl)) return -1;
+      const int32_t x = clc_first_ctaid_x(resp0 + 16u * slot);
+      ++taken;
+      if (warp_wide) __syncwarp();
+      if (arrive) {
+        if constexpr (CG == 1)
+          mbar_arrive(empty0 + 8u * slot);
+        else
+          mbar_arrive_cluster(mapa_shared(empty0 + 8u * slot, 0));
+      }
+      if (x < 0) {
+        finished = true;
+        started = false;
+        return 0;
+      }
+      it.start(x / CG);
+      if (issuer && !request(ctl)) return -1;
+    }
+  }
+
+  // After giving up: wait for the response of a request this thread issued
+  // and did not read, so that nothing lands in shared memory after exit.
+  __device__ bool drain(const WaitCtl& ctl) {
+    for (int32_t r = taken; r < requested; ++r) {
+      const uint32_t slot = (uint32_t)(r % SLOTS);
+      if (!mbar_wait<CG == 2>(full0 + 8u * slot, (uint32_t)((r / SLOTS) & 1), ctl)) return false;
+    }
+    return true;
+  }
+};
+
 template <int CG, int BN, int STAGES>
 __global__ void __launch_bounds__(192, 1)
     dense_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -94,6 +188,10 @@ __global__ void __launch_bounds__(192, 1)
   auto tfull_bar = [&](int b) -> uint32_t { return bars + 8u * (2 * STAGES + b); };
   auto tempty_bar = [&](int b) -> uint32_t { return bars + 8u * (2 * STAGES + 2 + b); };
   const uint32_t drain_bar = bars + 8u * (2 * STAGES + 4);
+  const uint32_t clc_full0 = bars + 8u * (2 * STAGES + 5);
+  const uint32_t clc_empty0 = clc_full0 + 8u * S::CLC_SLOTS;
+  const uint32_t clc_resp0 = base + S::CLC_OFF;
+  using Feed = IdFeed<CG, S::CLC_SLOTS>;
 
   const int warp = threadIdx.x / 32;
   const uint32_t lane = threadIdx.x % 32;
@@ -116,6 +214,12 @@ __global__ void __launch_bounds__(192, 1)
         mbar_init(tempty_bar(b), 4 * CG);  // every epilogue warp of the pair arrives
       }
       mbar_init(drain_bar, 1);
+      for (int i = 0; i < S::CLC_SLOTS; ++i) {
+        mbar_init(clc_full0 + 8u * i, 1);
+        // readers of every response: producer, MMA issuer and 4 epilogue warps
+        // of CTA 0, producer and 4 epilogue warps of CTA 1
+        mbar_init(clc_empty0 + 8u * i, CG == 2 ? 11 : 6);
+      }
       *abort_flag = 0u;
       fence_mbar_init();
       prefetch_tmap(&tmA);
@@ -150,9 +254,12 @@ __global__ void __launch_bounds__(192, 1)
       int64_t issued = 0;
       bool ok = true;
       const uint32_t full_rank0 = (CG == 2) ? mapa_shared(full_bar(0), 0) : full_bar(0);
-      WorkIter it(cluster, nclusters, args.dp_tiles, args.sk_units, args.k_blocks);
+      Feed feed(args, cluster, nclusters, clc_resp0, clc_full0, clc_empty0, rank == 0, false, true);
       WorkItem w;
-      while (ok && it.next(w)) {
+      for (;;) {
+        const int got = feed.next(w, ctl);
+        if (got < 0) ok = false;
+        if (got <= 0) break;
         trace_event(tb, kRoleProducer, kTraceItemBegin, w.tile, w.kb0);
         uint32_t stall = 0;
         const TileCoord tc = tile_coord(w.tile, args.tiles_m, args.tiles_n, args.group_m);
@@ -200,9 +307,14 @@ __global__ void __launch_bounds__(192, 1)
         }
         trace_event(tb, kRoleProducer, kTraceStall, w.tile, (int32_t)stall);
         trace_event(tb, kRoleProducer, kTraceItemEnd, w.tile, w.kb1);
+        if (!ok) break;
       }
       if (!ok) {
         report_timeout(args.status, kRoleProducer, abort_flag);
+        aborted = true;
+      }
+      if (!feed.drain(drain_ctl)) {
+        report_timeout(args.status, kRoleTeardown, abort_flag);
         aborted = true;
       }
       // Every load this CTA issued and signalled on its own barrier must land
@@ -232,9 +344,12 @@ __global__ void __launch_bounds__(192, 1)
       const uint32_t b_step = args.b_mn_major ? (kMNMajorStepBytes >> 4) : (kKMajorStepBytes >> 4);
       const uint32_t b_lbo = args.b_mn_major ? kMNMajorLBO : 16u;
       const uint32_t b_sbo = args.b_mn_major ? kMNMajorSBO : kKMajorSBO;
-      WorkIter it(cluster, nclusters, args.dp_tiles, args.sk_units, args.k_blocks);
+      Feed feed(args, cluster, nclusters, clc_resp0, clc_full0, clc_empty0, false, false, true);
       WorkItem w;
-      while (ok && it.next(w)) {
+      for (;;) {
+        const int got = feed.next(w, ctl);
+        if (got < 0) ok = false;
+        if (got <= 0) break;
         // Wait until the epilogue has drained this accumulator buffer.
         if (!mbar_wait<kCS>(tempty_bar(acc), acc_phase ^ 1u, ctl)) {
           ok = false;
@@ -353,13 +468,20 @@ __global__ void __launch_bounds__(192, 1)
 
     // Stream-K partial of cluster c, slot s, this CTA: BN/4 groups of 4 columns,
     // each [128 rows] of float4, so a warp's accesses are 512 contiguous bytes.
-    auto partial_of = [&](int64_t c, int s) -> float4* {
+    auto partial_of = [&](int64_t c, int s) -> float4* {  // c: stream-K range
       return reinterpret_cast<float4*>(args.partials + (((c * 2 + s) * CG + rank) * (int64_t)BN * 128));
     };
 
-    WorkIter it(cluster, nclusters, args.dp_tiles, args.sk_units, args.k_blocks);
+    Feed feed(args, cluster, nclusters, clc_resp0, clc_full0, clc_empty0, false, true, lane == 0);
     WorkItem w;
-    while (it.next(w)) {
+    for (;;) {
+      const int more = feed.next(w, ctl);
+      // The four epilogue warps read the same ids; they stop together.
+      if (named_bar_or(2, 128, more < 0)) {
+        ok = false;
+        break;
+      }
+      if (more == 0) break;
       const bool got = mbar_wait<kCS>(tfull_bar(acc), acc_phase, ctl);
       // The four epilogue warps meet at named barriers, so they give up together.
       if (named_bar_or(2, 128, !got)) {
@@ -392,14 +514,14 @@ __global__ void __launch_bounds__(192, 1)
         int32_t* const arrivals = args.tickets + tix;
         int32_t* const pubs = args.tickets + (int64_t)args.num_tiles * CG + tix;
         int64_t c_first, c_last;
-        sk_contributors(w.tile, args.dp_tiles, args.sk_units, args.k_blocks, nclusters, &c_first, &c_last);
+        sk_contributors(w.tile, args.dp_tiles, args.sk_units, args.k_blocks, args.sk_ranges, &c_first, &c_last);
         const int32_t others = (int32_t)(c_last - c_first);
         if (threadIdx.x == 64) *ticket_slot = atomicAdd(arrivals, 1);
         named_bar_sync(1, 128);
         const int32_t ticket = *ticket_slot;
         named_bar_sync(1, 128);
         if (ticket != others) {
-          float4* mine = partial_of(cluster, w.slot) + row;
+          float4* mine = partial_of(w.owner, w.slot) + row;
 #pragma unroll 1
           for (int c = 0; c < BN / 64; ++c) {
             float f[64];
@@ -426,7 +548,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
             for (int j = 0; j < 64; ++j) f[j] = 0.0f;
             for (int64_t cc = c_first; cc <= c_last; ++cc) {
-              if (cc == cluster) {
+              if (cc == w.owner) {
                 float own[64];
                 load_chunk(t_row, c, own);
                 if (c == BN / 64 - 1) release_tmem(acc);
@@ -434,7 +556,7 @@ __global__ void __launch_bounds__(192, 1)
                 for (int j = 0; j < 64; ++j) f[j] += own[j];
               } else if (have_all) {
                 const float4* src =
-                    partial_of(cc, sk_slot_of(cc, w.tile, args.dp_tiles, args.sk_units, args.k_blocks, nclusters)) +
+                    partial_of(cc, sk_slot_of(cc, w.tile, args.dp_tiles, args.sk_units, args.k_blocks, args.sk_ranges)) +
                     row;
                 float4 g[16];
 #pragma unroll

@@ -45,9 +45,11 @@ constexpr uint64_t kDrainTimeoutNs = 2000000ull;
 struct DenseArgs {
   int32_t M, N, K;
   int32_t tiles_m, tiles_n, num_tiles, k_blocks, group_m;
-  int32_t dp_tiles;  // tiles computed over the whole K range (round-robin), before the stream-K range
-  int64_t sk_units;  // (num_tiles - dp_tiles) * k_blocks, split evenly over the clusters
-  float* partials;   // stream-K partials [clusters][2][cta_group][BN/4][128] float4 (null if sk_units == 0)
+  int32_t dp_tiles;   // tiles computed over the whole K range
+  int32_t sk_ranges;  // stream-K ranges (work ids before the whole tiles); 0 without stream-K
+  int64_t sk_units;   // (num_tiles - dp_tiles) * k_blocks, split evenly over the ranges
+  int32_t dynamic;    // 1: one cluster per work id, ids taken over by cluster launch control
+  float* partials;    // stream-K partials [sk_ranges][2][cta_group][BN/4][128] float4 (null if sk_units == 0)
   int32_t* tickets;  // [2][num_tiles * cta_group] arrivals, publications; all zero between launches
   uint32_t idesc;
   int32_t b_mn_major;      // NN layout: B tile is MN-major in shared memory

@@ -190,6 +190,46 @@ __device__ __forceinline__ bool mbar_wait_stall(uint32_t bar, uint32_t parity, c
   return ok;
 }
 
+// ------------------------------------------------- cluster launch control ----
+// A request to cancel the launch of a cluster of this grid that has not
+// started yet.  The 16-byte response lands at `resp` (shared memory of this
+// CTA; with CG == 2 at the same offset in both CTAs of the pair) and
+// completes 16 transaction bytes on the barrier at the same offset.
+template <int CG>
+__device__ __forceinline__ void clc_try_cancel(uint32_t resp, uint32_t bar) {
+  if constexpr (CG == 1)
+    asm volatile("clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];" ::"r"(resp),
+                 "r"(bar)
+                 : "memory");
+  else
+    asm volatile(
+        "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.multicast::cluster::all.b128 [%0], [%1];" ::"r"(resp),
+        "r"(bar)
+        : "memory");
+}
+
+// Decodes a response: the x index of the first CTA of the cancelled cluster,
+// or -1 when no cluster was cancelled (the grid has none left to start).
+__device__ __forceinline__ int32_t clc_first_ctaid_x(uint32_t resp) {
+  int32_t x;
+  asm volatile(
+      "{\n\t.reg .b128 r;\n\t.reg .pred p;\n\t"
+      "ld.shared.b128 r, [%1];\n\t"
+      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
+      "mov.s32 %0, -1;\n\t"
+      "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %0, r;\n\t}"
+      : "=r"(x)
+      : "r"(resp)
+      : "memory");
+  return x;
+}
+
+// arrive + expect_tx on a barrier of another CTA of the cluster.
+__device__ __forceinline__ void mbar_arrive_expect_tx_cluster(uint32_t cluster_bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(cluster_bar), "r"(bytes)
+               : "memory");
+}
+
 // -------------------------------------------------------------------- TMA ----
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");

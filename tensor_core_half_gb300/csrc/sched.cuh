@@ -47,33 +47,56 @@ HG_HD int64_t splitk_owner(int64_t u, int64_t units, int64_t ctas) { return ((u 
 
 // One item of a cluster's work list: k-blocks [kb0, kb1) of tile `tile`.
 // slot < 0: the item covers the whole K range, its result goes straight to C.
-// slot 0 / 1: a stream-K partial; it is the first (0) or last (1) item of the
-// cluster's stream-K range, which fixes where its fp32 partial is kept.
+// slot 0 / 1: a stream-K partial; it is the first (0) or last (1) item of
+// stream-K range `owner`, which fixes where its fp32 partial is kept.
 struct WorkItem {
-  int32_t tile, kb0, kb1, slot;
+  int32_t tile, kb0, kb1, slot, owner;
 };
 
-// The persistent dense kernel's schedule ("Persistent kernel: static
-// scheduling", extended with stream-K).  Tiles [0, dp_tiles) are dealt
-// round-robin to the clusters and computed over the whole K range.  The
-// remaining tiles form sk_units = (num_tiles - dp_tiles) * k_blocks units of
-// one k-block each, cut into one contiguous range per cluster, so that every
-// cluster does the same number of k-blocks.  A tile cut between clusters is
-// finished by whichever contributor arrives last.  Each cluster walks its
-// stream-K range FIRST: the fix-ups of split tiles then overlap the mainloops
-// of the data-parallel tiles instead of ending the kernel.
+// The dense kernel's work, cut into work ids ("Persistent kernel: static
+// scheduling", extended with stream-K).  Ids [0, sk_ranges) are stream-K
+// ranges: the last tiles (num_tiles - dp_tiles of them) form sk_units =
+// (num_tiles - dp_tiles) * k_blocks units of one k-block each, cut into
+// sk_ranges contiguous ranges of equal size (up to one).  Ids [sk_ranges,
+// sk_ranges + dp_tiles) are whole tiles.  A tile cut between ranges is
+// finished by whichever contributor arrives last.
+//
+// Static schedule: cluster c of P walks ids c, c + P, c + 2P, ... with
+// sk_ranges = P, so that every cluster does the same number of k-blocks and
+// takes its stream-K range FIRST: the fix-ups of split tiles then overlap the
+// mainloops of the whole tiles instead of ending the kernel.  Dynamic
+// schedule: one cluster is launched per id; a running cluster that finishes
+// an id takes the id of a cluster that has not started yet (cluster launch
+// control), so the same ids are spread over the clusters that are running.
 struct WorkIter {
-  int32_t t, step, dp_tiles, k_blocks;
+  int32_t sk_ranges, dp_tiles, k_blocks;
+  int64_t sk_units;
+  int64_t id, step, n_ids;  // current id; the static walk's stride; id count
   int64_t u, u_begin, u_end;
+  int32_t dp_tile;  // whole tile still to hand out, or -1
 
-  HG_HD WorkIter(int32_t cluster, int32_t nclusters, int32_t dp_tiles_, int64_t sk_units, int32_t k_blocks_)
-      : t(cluster), step(nclusters), dp_tiles(dp_tiles_), k_blocks(k_blocks_) {
-    u_begin = splitk_begin(cluster, sk_units, nclusters);
-    u_end = splitk_begin((int64_t)cluster + 1, sk_units, nclusters);
-    u = u_begin;
+  HG_HD WorkIter(int32_t sk_ranges_, int32_t dp_tiles_, int64_t sk_units_, int32_t k_blocks_)
+      : sk_ranges(sk_units_ > 0 ? sk_ranges_ : 0), dp_tiles(dp_tiles_), k_blocks(k_blocks_), sk_units(sk_units_),
+        id(-1), step(0), u(0), u_begin(0), u_end(0), dp_tile(-1) {
+    n_ids = (int64_t)sk_ranges + dp_tiles;
   }
 
-  HG_HD bool next(WorkItem& w) {
+  // Make `id_` the current id (0 <= id_ < n_ids).
+  HG_HD void start(int64_t id_) {
+    id = id_;
+    if (id_ < sk_ranges) {
+      u_begin = splitk_begin(id_, sk_units, sk_ranges);
+      u_end = splitk_begin(id_ + 1, sk_units, sk_ranges);
+      u = u_begin;
+      dp_tile = -1;
+    } else {
+      u = u_begin = u_end = 0;
+      dp_tile = (int32_t)(id_ - sk_ranges);
+    }
+  }
+
+  // The next item of the current id; false once the id is used up.
+  HG_HD bool next_in_id(WorkItem& w) {
     if (u < u_end) {
       const int64_t rel = u / k_blocks;
       const int32_t kb0 = (int32_t)(u - rel * k_blocks);
@@ -84,34 +107,51 @@ struct WorkIter {
       w.kb0 = kb0;
       w.kb1 = kb1;
       w.slot = (kb0 == 0 && kb1 == k_blocks) ? -1 : (u == u_begin ? 0 : 1);
+      w.owner = (int32_t)id;
       u += kb1 - kb0;
       return true;
     }
-    if (t < dp_tiles) {
-      w.tile = t;
+    if (dp_tile >= 0) {
+      w.tile = dp_tile;
       w.kb0 = 0;
       w.kb1 = k_blocks;
       w.slot = -1;
-      t += step;
+      w.owner = -1;
+      dp_tile = -1;
       return true;
     }
     return false;
   }
+
+  // Static schedule of cluster `cluster` of `nclusters`.
+  HG_HD void start_static(int32_t cluster, int32_t nclusters) {
+    step = nclusters;
+    if (cluster < n_ids) start(cluster);
+  }
+
+  HG_HD bool next_static(WorkItem& w) {
+    if (id < 0) return false;
+    for (;;) {
+      if (next_in_id(w)) return true;
+      if (id + step >= n_ids) return false;
+      start(id + step);
+    }
+  }
 };
 
-// Contributors of stream-K tile `tile`: clusters [*first, *last], in K order.
-HG_HD void sk_contributors(int32_t tile, int32_t dp_tiles, int64_t sk_units, int32_t k_blocks, int32_t nclusters,
+// Contributors of stream-K tile `tile`: ranges [*first, *last], in K order.
+HG_HD void sk_contributors(int32_t tile, int32_t dp_tiles, int64_t sk_units, int32_t k_blocks, int32_t sk_ranges,
                            int64_t* first, int64_t* last) {
   const int64_t u0 = (int64_t)(tile - dp_tiles) * k_blocks;
-  *first = splitk_owner(u0, sk_units, nclusters);
-  *last = splitk_owner(u0 + k_blocks - 1, sk_units, nclusters);
+  *first = splitk_owner(u0, sk_units, sk_ranges);
+  *last = splitk_owner(u0 + k_blocks - 1, sk_units, sk_ranges);
 }
 
-// Where contributor `c` keeps its partial of stream-K tile `tile`: slot 0 if
-// the tile is the first of c's range, else slot 1 (it is then c's last).
+// Where range `c` keeps its partial of stream-K tile `tile`: slot 0 if the
+// tile is the first of c's range, else slot 1 (it is then c's last).
 HG_HD int32_t sk_slot_of(int64_t c, int32_t tile, int32_t dp_tiles, int64_t sk_units, int32_t k_blocks,
-                         int32_t nclusters) {
-  const int64_t first_tile = splitk_begin(c, sk_units, nclusters) / k_blocks;
+                         int32_t sk_ranges) {
+  const int64_t first_tile = splitk_begin(c, sk_units, sk_ranges) / k_blocks;
   return (first_tile == (int64_t)(tile - dp_tiles)) ? 0 : 1;
 }
 

@@ -58,6 +58,10 @@ HGEMM_OPT_GROUP_M = 4
 HGEMM_OPT_MAX_CTAS = 5
 HGEMM_OPT_STREAM_K = 6
 HGEMM_OPT_TRACE = 7
+HGEMM_OPT_SCHEDULE = 8
+HGEMM_SCHEDULE_STATIC = 0
+HGEMM_SCHEDULE_DYNAMIC = 1
+SCHEDULES = {"static": HGEMM_SCHEDULE_STATIC, "dynamic": HGEMM_SCHEDULE_DYNAMIC}
 
 LAYOUTS = {"TN": HGEMM_LAYOUT_TN, "NN": HGEMM_LAYOUT_NN}
 DTYPES = {"f16": HGEMM_F16, "bf16": HGEMM_BF16, "f32": HGEMM_F32}
@@ -70,7 +74,7 @@ class hgemm_plan_t(ctypes.Structure):
         "variant", "cta_group", "tile_m", "tile_n", "block_k", "stages", "tiles_m", "tiles_n", "num_tiles",
         "k_blocks", "grid", "group_m", "smem_bytes", "tmem_cols")] + [
         ("workspace_bytes", ctypes.c_int64), ("dp_tiles", ctypes.c_int32), ("stream_k", ctypes.c_int32),
-        ("sk_units", ctypes.c_int64)]
+        ("sk_units", ctypes.c_int64), ("sk_ranges", ctypes.c_int32), ("work_ids", ctypes.c_int32)]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -101,6 +105,8 @@ _lib.hgemm_plan.argtypes = [_i64, _i64, _i64, _i32, _i32, _i32, _i32, _i32, _i32
                             ctypes.POINTER(hgemm_plan_t)]
 _lib.hgemm_plan_work_item.restype = _i32
 _lib.hgemm_plan_work_item.argtypes = [ctypes.POINTER(hgemm_plan_t), _i32, _i32] + [ctypes.POINTER(_i32)] * 4
+_lib.hgemm_plan_id_item.restype = _i32
+_lib.hgemm_plan_id_item.argtypes = [ctypes.POINTER(hgemm_plan_t), _i32, _i32] + [ctypes.POINTER(_i32)] * 4
 _lib.hgemm_plan_tile.restype = _i32
 _lib.hgemm_plan_tile.argtypes = [ctypes.POINTER(hgemm_plan_t), _i32, ctypes.POINTER(_i32), ctypes.POINTER(_i32)]
 _lib.hgemm_plan_splitk_range.restype = _i32
@@ -199,6 +205,13 @@ def hgemm_plan_work_item(plan, cluster, index):
     t, a, b, s = _i32(), _i32(), _i32(), _i32()
     st = _lib.hgemm_plan_work_item(ctypes.byref(plan), int(cluster), int(index), ctypes.byref(t), ctypes.byref(a),
                                    ctypes.byref(b), ctypes.byref(s))
+    return int(st), t.value, a.value, b.value, s.value
+
+
+def hgemm_plan_id_item(plan, id, index):
+    t, a, b, s = _i32(), _i32(), _i32(), _i32()
+    st = _lib.hgemm_plan_id_item(ctypes.byref(plan), int(id), int(index), ctypes.byref(t), ctypes.byref(a),
+                                 ctypes.byref(b), ctypes.byref(s))
     return int(st), t.value, a.value, b.value, s.value
 
 

@@ -25,9 +25,10 @@ def h():
     handle.close()
 
 
-def run(h, a, b, M, N, K, layout, acc, out, variant="auto", C=None, stream_k=1):
+def run(h, a, b, M, N, K, layout, acc, out, variant="auto", C=None, stream_k=1, schedule="static"):
     h.set_option(hgemm.HGEMM_OPT_FORCE_VARIANT, hgemm.VARIANTS[variant])
     h.set_option(hgemm.HGEMM_OPT_STREAM_K, stream_k)
+    h.set_option(hgemm.HGEMM_OPT_SCHEDULE, hgemm.SCHEDULES[schedule])
     try:
         if layout == "NN" and variant in NN_UNSUPPORTED:
             A, B = a.cuda(), b.cuda()
@@ -44,6 +45,7 @@ def run(h, a, b, M, N, K, layout, acc, out, variant="auto", C=None, stream_k=1):
     finally:
         h.set_option(hgemm.HGEMM_OPT_FORCE_VARIANT, hgemm.HGEMM_VARIANT_AUTO)
         h.set_option(hgemm.HGEMM_OPT_STREAM_K, 1)
+        h.set_option(hgemm.HGEMM_OPT_SCHEDULE, hgemm.HGEMM_SCHEDULE_STATIC)
 
 
 @pytest.mark.parametrize("variant", ["auto"] + DENSE_VARIANTS)
@@ -181,6 +183,39 @@ def test_stream_k_small_integers_bit_exact(h, variant):
     assert np.array_equal(got, ref)
 
 
+# Dynamic schedule (cluster launch control).  Shapes with more work ids than
+# resident clusters, so that running clusters cancel pending ones and take
+# their ids, with and without stream-K ranges; plus a ragged shape.
+DYNAMIC_CASES = [("2sm256", 4096, 4096, 128, 1), ("2sm256", 4096, 4096, 128, 0), ("1sm128", 2048, 2048, 256, 0),
+                 ("1sm256", 2048, 4096, 192, 1), ("2sm192", 2048, 3072, 136, 1), ("2sm256", 1000, 3000, 4104, 1),
+                 ("1sm128", 130, 136, 72, 1)]
+
+
+@pytest.mark.parametrize("variant,M,N,K,sk", DYNAMIC_CASES)
+def test_dynamic_schedule_parity(h, variant, M, N, K, sk):
+    a, b, ab, bb = parity.inputs(M, N, K, "TN", "bf16", ("normal", 1.0), 81)
+    got = run(h, a, b, M, N, K, "TN", "f32", "bf16", variant, stream_k=sk, schedule="dynamic")
+    parity.check(got, ab, bb, M, N, K, "TN", "bf16", "f32", "bf16")
+    # the same ids with the same contents: bitwise equal to the static schedule
+    ref = run(h, a, b, M, N, K, "TN", "f32", "bf16", variant, stream_k=sk, schedule="static")
+    assert np.array_equal(got, ref)
+    again = run(h, a, b, M, N, K, "TN", "f32", "bf16", variant, stream_k=sk, schedule="dynamic")
+    assert np.array_equal(got, again)
+
+
+@pytest.mark.parametrize("variant", ["2sm256", "1sm128"])
+def test_dynamic_schedule_nn_f16_acc_and_integers(h, variant):
+    M, N, K = 2048, 2560, 1024
+    a, b, ab, bb = parity.inputs(M, N, K, "NN", "f16", ("uniform", -1.0, 1.0), 82)
+    got = run(h, a, b, M, N, K, "NN", "f16", "f16", variant, schedule="dynamic")
+    parity.check(got, ab, bb, M, N, K, "NN", "f16", "f16", "f16")
+    M, N, K = 2048, 2048, 1024
+    a, b, ab, bb = parity.inputs(M, N, K, "TN", "bf16", ("int", -4, 4), 83)
+    got = run(h, a, b, M, N, K, "TN", "f32", "bf16", variant, schedule="dynamic")
+    ref, _, _ = oracle.gemm(ab, bb, M, N, K, "TN", "bf16", "bf16")
+    assert np.array_equal(got, ref)
+
+
 @pytest.mark.parametrize("variant,M,N,K", [("2sm256", 300, 264, 200), ("1sm128", 130, 136, 72),
                                            ("splitk", 17, 520, 200), ("1sm256", 1, 8, 8)])
 def test_guard_bands_untouched(h, variant, M, N, K):
@@ -246,8 +281,10 @@ def test_argument_validation(h):
     assert torch.all(C == 0)  # nothing was launched
 
 
-@pytest.mark.parametrize("variant,M", [("1sm128", 512), ("2sm256", 512), ("splitk", 16)])
-def test_bounded_wait_gives_up_and_recovers(h, variant, M):
+@pytest.mark.parametrize("variant,M,schedule", [("1sm128", 512, "static"), ("2sm256", 512, "static"),
+                                                ("splitk", 16, "static"), ("1sm128", 4096, "dynamic"),
+                                                ("2sm256", 4096, "dynamic")])
+def test_bounded_wait_gives_up_and_recovers(h, variant, M, schedule):
     # The first CTA's producer drops its first stage; the MMA warp's wait on that
     # stage can never succeed, gives up after the limit, and every role exits.
     N, K = 1024, 1024
@@ -257,6 +294,7 @@ def test_bounded_wait_gives_up_and_recovers(h, variant, M):
     h.set_option(hgemm.HGEMM_OPT_FORCE_VARIANT, hgemm.VARIANTS[variant])
     h.set_option(hgemm.HGEMM_OPT_TIMEOUT_NS, 20_000_000)
     h.set_option(hgemm.HGEMM_OPT_INJECT_FAULT, 1)
+    h.set_option(hgemm.HGEMM_OPT_SCHEDULE, hgemm.SCHEDULES[schedule])
     try:
         h.run(A, B, C, layout="TN", acc="f32")
         st, detail = h.sync_status()
@@ -266,8 +304,9 @@ def test_bounded_wait_gives_up_and_recovers(h, variant, M):
         h.set_option(hgemm.HGEMM_OPT_INJECT_FAULT, 0)
         h.set_option(hgemm.HGEMM_OPT_TIMEOUT_NS, 2_000_000_000)
         h.set_option(hgemm.HGEMM_OPT_FORCE_VARIANT, hgemm.HGEMM_VARIANT_AUTO)
+        h.set_option(hgemm.HGEMM_OPT_SCHEDULE, hgemm.HGEMM_SCHEDULE_STATIC)
     # the context is still usable and the next launch is correct
-    got = run(h, a, b, M, N, K, "TN", "f32", "bf16", variant)
+    got = run(h, a, b, M, N, K, "TN", "f32", "bf16", variant, schedule=schedule)
     parity.check(got, ab, bb, M, N, K, "TN", "bf16", "f32", "bf16")
 
 

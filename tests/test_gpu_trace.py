@@ -65,3 +65,45 @@ def _partial_tiles(p, c):
         if slot >= 0:
             out.append(t)
         i += 1
+
+
+@pytest.mark.parametrize("variant,M,N,K,sk", [("2sm256", 4096, 4096, 256, 1), ("1sm128", 2048, 4096, 128, 0)])
+def test_dynamic_schedule_takes_over_pending_clusters(variant, M, N, K, sk):
+    """Under the dynamic schedule one cluster is launched per work id, but the
+    clusters that start first cancel the launch of the others and run their
+    ids: fewer CTAs begin than were launched, and every id's items appear
+    exactly once."""
+    with hgemm.Handle() as h:
+        h.set_option(hgemm.HGEMM_OPT_FORCE_VARIANT, hgemm.VARIANTS[variant])
+        h.set_option(hgemm.HGEMM_OPT_STREAM_K, sk)
+        h.set_option(hgemm.HGEMM_OPT_SCHEDULE, hgemm.HGEMM_SCHEDULE_DYNAMIC)
+        h.set_option(hgemm.HGEMM_OPT_TRACE, 1 << 18)
+        a, b, _, _ = parity.inputs(M, N, K, "TN", "bf16", ("normal", 1.0), 72)
+        A, B = a.cuda(), b.cuda()
+        C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        h.run(A, B, C, layout="TN", acc="f32")
+        assert h.sync_status()[0] == hgemm.HGEMM_OK
+        st, n, rows = hgemm.hgemm_trace_read(h.h, 1 << 18)
+        assert st == hgemm.HGEMM_OK and n == len(rows) > 0
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    st, p = hgemm.hgemm_plan(M, N, K, 0, hgemm.HGEMM_BF16, hgemm.HGEMM_F32, hgemm.HGEMM_BF16, sms,
+                             hgemm.VARIANTS[variant], 0, sk)
+    launched = p.work_ids * p.cta_group
+    began = collections.Counter(r[1] for r in rows if r[2] == 0 and r[3] == 1)
+    assert p.work_ids > p.grid // p.cta_group  # more ids than resident clusters
+    assert 0 < len(began) <= p.grid < launched  # only resident CTAs ran; the rest were cancelled
+    expect = collections.Counter()
+    for i in range(p.work_ids):
+        j = 0
+        while True:
+            s, t, a0, b0, slot = hgemm.hgemm_plan_id_item(p, i, j)
+            if s != 0:
+                break
+            expect[(t, a0, b0)] += 1
+            j += 1
+    # MMA issuer items (one per cluster): item_begin carries (tile, kb0), item_end (tile, kb1)
+    got = collections.Counter()
+    for sp in trace.spans(rows):
+        if sp["role"] == "mma":
+            got[(sp["tile"], sp["begin_value"], sp["end_value"])] += 1
+    assert got == expect

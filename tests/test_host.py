@@ -219,6 +219,69 @@ def test_work_lists_cover_every_unit_once(M, N, K, variant):
             assert set(owners) == set(range(owners[0], owners[-1] + 1))
 
 
+@pytest.mark.parametrize("M,N,K,variant", STREAMK_CASES)
+def test_work_ids_partition_the_work(M, N, K, variant):
+    """The dynamic schedule runs whole work ids in any order: the ids must cut
+    the work into disjoint pieces that cover it, the static walk of cluster c
+    must be exactly ids c, c + P, ... in order, and the stream-K ranges must
+    come first."""
+    st, p = plan(M, N, K, variant=variant)
+    assert st == ST_OK
+    clusters = p.grid // p.cta_group
+    assert p.work_ids == p.sk_ranges + p.dp_tiles
+    assert p.sk_ranges == (clusters if p.stream_k else 0)
+    items = {}
+    covered = set()
+    for i in range(p.work_ids):
+        lst, j = [], 0
+        while True:
+            s, t, a, b, slot = H.hgemm_plan_id_item(p, i, j)
+            if s != ST_OK:
+                break
+            lst.append((t, a, b, slot))
+            for kb in range(a, b):
+                assert (t, kb) not in covered
+                covered.add((t, kb))
+            j += 1
+        assert lst, "every id has work"
+        if i >= p.sk_ranges:
+            assert lst == [(i - p.sk_ranges, 0, p.k_blocks, -1)]
+        else:
+            assert all(t >= p.dp_tiles for t, _, _, _ in lst)
+            # slot 0 only on the first piece, slot 1 only on the last
+            for k, (t, a, b, slot) in enumerate(lst):
+                if slot == 0:
+                    assert k == 0
+                if slot == 1:
+                    assert k == len(lst) - 1 and k > 0
+        items[i] = lst
+    assert len(covered) == p.num_tiles * p.k_blocks
+    for c in range(clusters):
+        walk, j = [], 0
+        while True:
+            s, t, a, b, slot = H.hgemm_plan_work_item(p, c, j)
+            if s != ST_OK:
+                break
+            walk.append((t, a, b, slot))
+            j += 1
+        expect = [it for i in range(c, p.work_ids, clusters) for it in items[i]]
+        assert walk == expect
+
+
+def test_work_id_arguments():
+    st, p = plan(4096, 4096, 4096)
+    assert H.hgemm_plan_id_item(p, -1, 0)[0] == ST_INV
+    assert H.hgemm_plan_id_item(p, p.work_ids, 0)[0] == ST_INV
+    assert H.hgemm_plan_id_item(p, 0, -1)[0] == ST_INV
+    st, sp = plan(16, 16384, 8192)
+    assert H.hgemm_plan_id_item(sp, 0, 0)[0] == ST_INV
+
+
+def test_schedule_option_values():
+    # no device here: only the option's validation path is reachable without a handle
+    assert H.SCHEDULES == {"static": 0, "dynamic": 1}
+
+
 def test_work_list_arguments():
     st, p = plan(4096, 4096, 4096)
     assert H.hgemm_plan_work_item(p, -1, 0)[0] == ST_INV
