@@ -75,8 +75,21 @@ typedef enum {
                                   dense tiles along K (stream-K); 0 keeps every tile whole    */
   HGEMM_OPT_TRACE = 7,         /* value: capacity in events of a device trace buffer that the
                                   kernels append to (0 = off, the default); hgemm_trace_read */
-  HGEMM_OPT_SCHEDULE = 8       /* value: an hgemm_schedule_t for the dense kernels           */
+  HGEMM_OPT_SCHEDULE = 8,      /* value: an hgemm_schedule_t for the dense kernels           */
+  HGEMM_OPT_EPILOGUE = 9       /* value: an hgemm_epilogue_t for the dense kernels           */
 } hgemm_option_t;
+
+/*
+ * How the dense kernels' epilogue writes C (HGEMM_OPT_EPILOGUE); both give
+ * the same bits.
+ *   TMA_STORE (default): tcgen05.ld -> round -> 128-byte-swizzled shared
+ *     staging (per warp, double-buffered) -> TMA tensor store of 32 x 64 boxes.
+ *   DIRECT: tcgen05.ld -> round -> 16-byte global stores from registers, each
+ *     thread writing its own row, as the first kernel of "tcgen05 for
+ *     dummies: a B200 GEMM from scratch" (translated) writes its tile back;
+ *     that page reports plain stores beating its TMA store.
+ */
+typedef enum { HGEMM_EPILOGUE_TMA_STORE = 0, HGEMM_EPILOGUE_DIRECT = 1 } hgemm_epilogue_t;
 
 /*
  * Dense work schedules (HGEMM_OPT_SCHEDULE).  Both cut the same work into

@@ -48,6 +48,7 @@ struct Ctx {
   int max_ctas = 0;
   bool stream_k = true;
   int schedule = HGEMM_SCHEDULE_STATIC;
+  int epilogue = HGEMM_EPILOGUE_TMA_STORE;
   TraceBuf* trace = nullptr;  // device trace buffer (HGEMM_OPT_TRACE)
   int64_t trace_capacity = 0;
   // hgemm_run_host: two staging sets (double buffering across calls), three
@@ -491,6 +492,10 @@ hgemm_status_t hgemm_set_option(hgemm_handle_t h, int32_t option, int64_t value)
       if (value != HGEMM_SCHEDULE_STATIC && value != HGEMM_SCHEDULE_DYNAMIC) return HGEMM_ERR_INVALID_ARG;
       h->schedule = (int)value;
       return HGEMM_OK;
+    case HGEMM_OPT_EPILOGUE:
+      if (value != HGEMM_EPILOGUE_TMA_STORE && value != HGEMM_EPILOGUE_DIRECT) return HGEMM_ERR_INVALID_ARG;
+      h->epilogue = (int)value;
+      return HGEMM_OK;
     case HGEMM_OPT_TRACE: {
       if (value < 0 || value > (int64_t)1 << 26) return HGEMM_ERR_INVALID_ARG;
       if (h->trace) {
@@ -599,6 +604,8 @@ hgemm_status_t hgemm_run(hgemm_handle_t h, const void* A, const void* B, void* C
   args.sk_ranges = p.sk_ranges;
   args.sk_units = p.sk_units;
   args.dynamic = h->schedule == HGEMM_SCHEDULE_DYNAMIC ? 1 : 0;
+  args.epi_direct = h->epilogue == HGEMM_EPILOGUE_DIRECT ? 1 : 0;
+  args.C = C;
   args.partials = nullptr;
   args.tickets = nullptr;
   if (p.stream_k) {

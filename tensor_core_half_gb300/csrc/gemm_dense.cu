@@ -410,6 +410,7 @@ __global__ void __launch_bounds__(192, 1)
     bool ok = true;
     const bool out_bf16 = args.out_bf16 != 0;
     const bool acc_f16 = args.acc_f16 != 0;
+    const bool epi_direct = args.epi_direct != 0;
 
     // 64 accumulator columns of this thread's row, as fp32.
     auto load_chunk = [&](uint32_t t_row, int c, float (&f)[64]) {
@@ -437,6 +438,18 @@ __global__ void __launch_bounds__(192, 1)
       } else {
 #pragma unroll
         for (int i = 0; i < 32; ++i) p[i] = pack_f32x2_to_f16x2(f[2 * i], f[2 * i + 1]);
+      }
+      if (epi_direct) {
+        // Straight from registers: this thread's row, eight 16-byte pieces
+        // (N is a multiple of 8, so a piece is wholly inside C or outside).
+        const int r = m0 + (int)lane;
+        if (r < args.M) {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(args.C) + (size_t)r * (size_t)args.N + nc);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            if (nc + 8 * j < args.N) dst[j] = make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
+        }
+        return;
       }
       const uint32_t buf = epi + (uint32_t)(ew * 2 + (int)(nstores & 1u)) * S::EPI_BOX_BYTES;
       if (lane == 0) bulk_wait_read<1>();  // the store that last used this buffer has read it

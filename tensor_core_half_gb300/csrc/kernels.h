@@ -49,6 +49,8 @@ struct DenseArgs {
   int32_t sk_ranges;  // stream-K ranges (work ids before the whole tiles); 0 without stream-K
   int64_t sk_units;   // (num_tiles - dp_tiles) * k_blocks, split evenly over the ranges
   int32_t dynamic;    // 1: one cluster per work id, ids taken over by cluster launch control
+  int32_t epi_direct; // 1: the epilogue stores C from registers (16-byte stores), no TMA store
+  void* C;            // [M][N] row-major output (used by the direct epilogue)
   float* partials;    // stream-K partials [sk_ranges][2][cta_group][BN/4][128] float4 (null if sk_units == 0)
   int32_t* tickets;  // [2][num_tiles * cta_group] arrivals, publications; all zero between launches
   uint32_t idesc;

@@ -62,6 +62,10 @@ HGEMM_OPT_SCHEDULE = 8
 HGEMM_SCHEDULE_STATIC = 0
 HGEMM_SCHEDULE_DYNAMIC = 1
 SCHEDULES = {"static": HGEMM_SCHEDULE_STATIC, "dynamic": HGEMM_SCHEDULE_DYNAMIC}
+HGEMM_OPT_EPILOGUE = 9
+HGEMM_EPILOGUE_TMA_STORE = 0
+HGEMM_EPILOGUE_DIRECT = 1
+EPILOGUES = {"tma": HGEMM_EPILOGUE_TMA_STORE, "direct": HGEMM_EPILOGUE_DIRECT}
 
 LAYOUTS = {"TN": HGEMM_LAYOUT_TN, "NN": HGEMM_LAYOUT_NN}
 DTYPES = {"f16": HGEMM_F16, "bf16": HGEMM_BF16, "f32": HGEMM_F32}

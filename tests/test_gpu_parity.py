@@ -25,10 +25,11 @@ def h():
     handle.close()
 
 
-def run(h, a, b, M, N, K, layout, acc, out, variant="auto", C=None, stream_k=1, schedule="static"):
+def run(h, a, b, M, N, K, layout, acc, out, variant="auto", C=None, stream_k=1, schedule="static", epilogue="tma"):
     h.set_option(hgemm.HGEMM_OPT_FORCE_VARIANT, hgemm.VARIANTS[variant])
     h.set_option(hgemm.HGEMM_OPT_STREAM_K, stream_k)
     h.set_option(hgemm.HGEMM_OPT_SCHEDULE, hgemm.SCHEDULES[schedule])
+    h.set_option(hgemm.HGEMM_OPT_EPILOGUE, hgemm.EPILOGUES[epilogue])
     try:
         if layout == "NN" and variant in NN_UNSUPPORTED:
             A, B = a.cuda(), b.cuda()
@@ -46,6 +47,7 @@ def run(h, a, b, M, N, K, layout, acc, out, variant="auto", C=None, stream_k=1, 
         h.set_option(hgemm.HGEMM_OPT_FORCE_VARIANT, hgemm.HGEMM_VARIANT_AUTO)
         h.set_option(hgemm.HGEMM_OPT_STREAM_K, 1)
         h.set_option(hgemm.HGEMM_OPT_SCHEDULE, hgemm.HGEMM_SCHEDULE_STATIC)
+        h.set_option(hgemm.HGEMM_OPT_EPILOGUE, hgemm.HGEMM_EPILOGUE_TMA_STORE)
 
 
 @pytest.mark.parametrize("variant", ["auto"] + DENSE_VARIANTS)
@@ -216,6 +218,39 @@ def test_dynamic_schedule_nn_f16_acc_and_integers(h, variant):
     assert np.array_equal(got, ref)
 
 
+# Direct-store epilogue: same bits as the TMA-store epilogue, ragged edges
+# clipped by the stores' own bounds checks.
+DIRECT_CASES = [("1sm128", "TN", 1000, 1000, 1024, ("bf16", "f32", "bf16")),
+                ("1sm256", "NN", 129, 264, 640, ("f16", "f32", "f16")),
+                ("2sm256", "TN", 1024, 1280, 1024, ("bf16", "f32", "bf16")),
+                ("2sm256", "NN", 768, 520, 4104, ("f16", "f16", "f16")),
+                ("2sm192", "TN", 1000, 3000, 4104, ("bf16", "f32", "f16")),
+                ("2sm256", "TN", 1, 8, 8, ("bf16", "f32", "bf16"))]
+
+
+@pytest.mark.parametrize("variant,layout,M,N,K,combo", DIRECT_CASES)
+def test_direct_epilogue_parity(h, variant, layout, M, N, K, combo):
+    fin, acc, out = combo
+    a, b, ab, bb = parity.inputs(M, N, K, layout, fin, ("uniform", -1.0, 1.0), 84)
+    got = run(h, a, b, M, N, K, layout, acc, out, variant, epilogue="direct")
+    parity.check(got, ab, bb, M, N, K, layout, fin, acc, out)
+    ref = run(h, a, b, M, N, K, layout, acc, out, variant, epilogue="tma")
+    assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("variant,M,N,K", [("2sm256", 300, 264, 200), ("1sm128", 130, 136, 72),
+                                           ("2sm192", 257, 392, 136)])
+def test_direct_epilogue_guard_bands_untouched(h, variant, M, N, K):
+    a, b, ab, bb = parity.inputs(M, N, K, "TN", "bf16", ("normal", 1.0), 85)
+    pad = 4096
+    buf = torch.full((pad + M * N + pad,), 0x7E7E, dtype=torch.int16, device="cuda")
+    C = buf[pad:pad + M * N].view(torch.bfloat16).view(M, N)
+    got = run(h, a, b, M, N, K, "TN", "f32", "bf16", variant, C=C, epilogue="direct", schedule="dynamic")
+    parity.check(got, ab, bb, M, N, K, "TN", "bf16", "f32", "bf16")
+    host = buf.cpu().numpy()
+    assert np.all(host[:pad] == 0x7E7E) and np.all(host[pad + M * N:] == 0x7E7E)
+
+
 @pytest.mark.parametrize("variant,M,N,K", [("2sm256", 300, 264, 200), ("1sm128", 130, 136, 72),
                                            ("splitk", 17, 520, 200), ("1sm256", 1, 8, 8)])
 def test_guard_bands_untouched(h, variant, M, N, K):
@@ -305,6 +340,7 @@ def test_bounded_wait_gives_up_and_recovers(h, variant, M, schedule):
         h.set_option(hgemm.HGEMM_OPT_TIMEOUT_NS, 2_000_000_000)
         h.set_option(hgemm.HGEMM_OPT_FORCE_VARIANT, hgemm.HGEMM_VARIANT_AUTO)
         h.set_option(hgemm.HGEMM_OPT_SCHEDULE, hgemm.HGEMM_SCHEDULE_STATIC)
+        h.set_option(hgemm.HGEMM_OPT_EPILOGUE, hgemm.HGEMM_EPILOGUE_TMA_STORE)
     # the context is still usable and the next launch is correct
     got = run(h, a, b, M, N, K, "TN", "f32", "bf16", variant, schedule=schedule)
     parity.check(got, ab, bb, M, N, K, "TN", "bf16", "f32", "bf16")
