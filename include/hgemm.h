@@ -330,6 +330,73 @@ uint64_t hgemm_encode_smem_desc(uint32_t smem_addr, uint32_t lbo_bytes, uint32_t
 hgemm_status_t hgemm_run_splitk_noalloc(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
                                         hgemm_dtype_t in_dtype, hgemm_dtype_t out_dtype, void* stream);
 
+/* ------------------------------------------------------------------------- */
+/* TMA-engine micro-benchmark.                                                */
+
+/*
+ * How one tile of tile_rows x tile_cols bf16 elements is copied global ->
+ * shared.  "tcgen05 for dummies: a B200 GEMM from scratch" (translated)
+ * compares 16-byte and 128-byte inner boxes, each as several 2-D copies or
+ * one 3-D copy per tile (its v1a/v1b and v2a/v2b kernels), and in its section
+ * on the 128-byte swizzle asks for a micro-benchmark of the TMA engine.
+ */
+typedef enum {
+  HGEMM_TMA_2D_16B = 0,  /* tile_cols / 8 copies of a {8, tile_rows} box, no swizzle          */
+  HGEMM_TMA_3D_16B = 1,  /* one copy of a {8, tile_rows, tile_cols / 8} box, no swizzle       */
+  HGEMM_TMA_2D_128B = 2, /* tile_cols / 64 copies of a {64, tile_rows} box, 128-byte swizzle  */
+  HGEMM_TMA_3D_128B = 3, /* one copy of a {64, tile_rows, tile_cols / 64} box, 128-byte swizzle */
+  HGEMM_TMA_BULK = 4     /* one 1-D bulk copy of the tile's bytes (tiles stored back to back) */
+} hgemm_tma_mode_t;
+
+typedef struct {
+  int32_t mode;       /* hgemm_tma_mode_t                                                    */
+  int32_t tile_rows;  /* 8..256, a multiple of 8                                              */
+  int32_t tile_cols;  /* a multiple of 8 (of 64 for the 128-byte modes; <= 2048 for 3D_16B)   */
+  int32_t depth;      /* tiles in flight per CTA (shared-memory slots), 1..8                  */
+  int32_t issuers;    /* warps issuing a tile's copies, 1 or 2 (<= copies per tile)           */
+  int32_t ctas;       /* CTAs, one per SM; 0 = every SM                                       */
+  int32_t iters;      /* tiles each CTA copies                                                */
+  int32_t walk;       /* hgemm_tma_walk_t: the order in which a CTA visits tiles              */
+} hgemm_tma_bench_config_t;
+
+typedef enum {
+  HGEMM_TMA_WALK_SCATTERED = 0, /* CTA c, round j: tile (c * 7919 + j * 13) mod n_tiles          */
+  HGEMM_TMA_WALK_ALONG_K = 1    /* CTA c stays on row band c mod tiles_y and takes its column
+                                   tiles in order from ((c / tiles_y) * 7) mod tiles_x, the way a
+                                   GEMM's producer walks K over the same rows of A            */
+} hgemm_tma_walk_t;
+
+typedef struct {
+  double ms;               /* event-timed kernel duration                                     */
+  double bytes;            /* bytes copied by all CTAs                                        */
+  double gbs;              /* bytes / ms, GB/s                                                */
+  double bytes_per_clk_sm; /* median over CTAs of the CTA's bytes / its SM cycles             */
+  double sm_mhz;           /* median SM clock seen by the CTAs                                */
+  int32_t copies_per_tile;
+  int32_t ctas;
+  int32_t tile_bytes;
+  int32_t reserved;
+} hgemm_tma_bench_result_t;
+
+/*
+ * hgemm_tma_bench -- every CTA copies cfg->iters tiles of `src` (device
+ * pointer, height x width bf16 row-major, 128-byte aligned; height a
+ * multiple of tile_rows, width of tile_cols; for BULK the same bytes are read
+ * as height*width/(tile_rows*tile_cols) tiles stored one after another) into
+ * a ring of cfg->depth shared-memory slots, visiting tiles in the order
+ * cfg->walk gives (tiles numbered row-major over the height/tile_rows x
+ * width/tile_cols grid).  Synchronous: returns after
+ * the kernel, with *res filled.  Checks: sums (host, 2 per CTA, nullable)
+ * receives the sum of the 16-bit words in the CTA's slots after the last
+ * round and the sum of their squares; last_tiles (host, depth per CTA,
+ * nullable) the tile index each slot held (-1 if unused), so the caller can
+ * recompute both sums.  Allocates a small result buffer with cudaMalloc.
+ * INVALID_ARG / MISALIGNED / UNSUPPORTED (slots do not fit in shared memory)
+ * before any launch; TIMEOUT if a bounded wait gave up.
+ */
+hgemm_status_t hgemm_tma_bench(const void* src, int64_t height, int64_t width, const hgemm_tma_bench_config_t* cfg,
+                               hgemm_tma_bench_result_t* res, uint64_t* sums, int32_t* last_tiles, void* stream);
+
 /* Library version, e.g. 100 for 0.1.0. */
 int32_t hgemm_version(void);
 

@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libhgemm.so")
-SOURCES = ["api.cu", "gemm_dense.cu", "gemm_splitk.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "gemm_dense.cu", "gemm_splitk.cu", "noalloc.cu", "tma_bench.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

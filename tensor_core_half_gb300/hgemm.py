@@ -111,6 +111,9 @@ _lib.hgemm_plan_work_item.restype = _i32
 _lib.hgemm_plan_work_item.argtypes = [ctypes.POINTER(hgemm_plan_t), _i32, _i32] + [ctypes.POINTER(_i32)] * 4
 _lib.hgemm_plan_id_item.restype = _i32
 _lib.hgemm_plan_id_item.argtypes = [ctypes.POINTER(hgemm_plan_t), _i32, _i32] + [ctypes.POINTER(_i32)] * 4
+_lib.hgemm_tma_bench.restype = _i32
+_lib.hgemm_tma_bench.argtypes = [_vp, _i64, _i64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                 _vp]
 _lib.hgemm_plan_tile.restype = _i32
 _lib.hgemm_plan_tile.argtypes = [ctypes.POINTER(hgemm_plan_t), _i32, ctypes.POINTER(_i32), ctypes.POINTER(_i32)]
 _lib.hgemm_plan_splitk_range.restype = _i32
@@ -217,6 +220,45 @@ def hgemm_plan_id_item(plan, id, index):
     st = _lib.hgemm_plan_id_item(ctypes.byref(plan), int(id), int(index), ctypes.byref(t), ctypes.byref(a),
                                  ctypes.byref(b), ctypes.byref(s))
     return int(st), t.value, a.value, b.value, s.value
+
+
+HGEMM_TMA_2D_16B, HGEMM_TMA_3D_16B, HGEMM_TMA_2D_128B, HGEMM_TMA_3D_128B, HGEMM_TMA_BULK = range(5)
+TMA_MODES = {"2d_16b": HGEMM_TMA_2D_16B, "3d_16b": HGEMM_TMA_3D_16B, "2d_128b": HGEMM_TMA_2D_128B,
+             "3d_128b": HGEMM_TMA_3D_128B, "bulk": HGEMM_TMA_BULK}
+
+
+class hgemm_tma_bench_config_t(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("mode", "tile_rows", "tile_cols", "depth", "issuers", "ctas", "iters",
+                                              "walk")]
+
+
+class hgemm_tma_bench_result_t(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_double) for n in ("ms", "bytes", "gbs", "bytes_per_clk_sm", "sm_mhz")] + [
+        (n, ctypes.c_int32) for n in ("copies_per_tile", "ctas", "tile_bytes", "reserved")]
+
+    def as_dict(self):
+        return {n: getattr(self, n) for n, _ in self._fields_ if n != "reserved"}
+
+
+HGEMM_TMA_WALK_SCATTERED, HGEMM_TMA_WALK_ALONG_K = 0, 1
+TMA_WALKS = {"scattered": HGEMM_TMA_WALK_SCATTERED, "along_k": HGEMM_TMA_WALK_ALONG_K}
+
+
+def hgemm_tma_bench(src_ptr, height, width, mode, tile_rows, tile_cols, depth, iters, issuers=1, ctas=0, stream=0,
+                    max_ctas=1024, walk=0):
+    """Runs the TMA micro-benchmark (synchronous).  Returns (status, result,
+    sums [ctas][2], last_tiles [ctas][depth]) with plain Python containers."""
+    cfg = hgemm_tma_bench_config_t(int(mode), int(tile_rows), int(tile_cols), int(depth), int(issuers), int(ctas),
+                                   int(iters), int(walk))
+    res = hgemm_tma_bench_result_t()
+    n = max_ctas if ctas == 0 else int(ctas)
+    sums = (ctypes.c_uint64 * (2 * n))()
+    last = (ctypes.c_int32 * (max(1, int(depth)) * n))()
+    st = _lib.hgemm_tma_bench(src_ptr, int(height), int(width), ctypes.byref(cfg), ctypes.byref(res), sums, last,
+                              stream)
+    got = res.ctas if st == HGEMM_OK else 0
+    return (int(st), res, [(sums[2 * i], sums[2 * i + 1]) for i in range(got)],
+            [list(last[i * depth:(i + 1) * depth]) for i in range(got)])
 
 
 def hgemm_plan_tile(plan, t):

@@ -282,6 +282,28 @@ def test_schedule_option_values():
     assert H.SCHEDULES == {"static": 0, "dynamic": 1}
 
 
+def test_tma_bench_validates_before_touching_the_device():
+    fake = 1 << 20  # never dereferenced: every case below is rejected or finds no device
+    assert H.hgemm_tma_bench(None, 1024, 1024, 0, 128, 64, 2, 8)[0] == ST_INV
+    assert H.hgemm_tma_bench(fake, 1024, 1024, 5, 128, 64, 2, 8)[0] == ST_INV
+    assert H.hgemm_tma_bench(fake, 1000, 1024, 0, 128, 64, 2, 8)[0] == ST_INV  # height % tile_rows
+    assert H.hgemm_tma_bench(fake, 1024, 1024, 2, 128, 32, 2, 8)[0] == ST_INV  # 128-byte box needs 64 columns
+    assert H.hgemm_tma_bench(fake + 64, 1024, 1024, 0, 128, 64, 2, 8)[0] == H.HGEMM_ERR_MISALIGNED
+    assert H.hgemm_tma_bench(fake, 1024, 1024, 0, 128, 64, 2, 8)[0] == H.HGEMM_ERR_NO_DEVICE
+
+
+def test_tma_bench_reference_sums():
+    from tensor_core_half_gb300 import tma_bench
+    import numpy as np
+    words = tma_bench.source(64, 256, device="cpu").view(torch.int16).numpy().view(np.uint16).astype(np.uint64)
+    # tile 3 of a 32 x 64 grid is rows 0..31, columns 192..255
+    t = words[0:32, 192:256]
+    assert tma_bench.expected_sums(64, 256, H.HGEMM_TMA_2D_128B, 32, 64, [3, -1]) == (int(t.sum()), int((t * t).sum()))
+    # bulk tile 1: the second 2048 words in memory order
+    f = words.reshape(-1)[2048:4096]
+    assert tma_bench.expected_sums(64, 256, H.HGEMM_TMA_BULK, 32, 64, [1]) == (int(f.sum()), int((f * f).sum()))
+
+
 def test_work_list_arguments():
     st, p = plan(4096, 4096, 4096)
     assert H.hgemm_plan_work_item(p, -1, 0)[0] == ST_INV
