@@ -92,9 +92,13 @@ typedef enum {
 typedef enum { HGEMM_EPILOGUE_TMA_STORE = 0, HGEMM_EPILOGUE_DIRECT = 1 } hgemm_epilogue_t;
 
 /*
- * Dense work schedules (HGEMM_OPT_SCHEDULE).  Both cut the same work into
- * the same work ids (hgemm_plan_t: sk_ranges stream-K ranges, then dp_tiles
- * whole tiles) and give bitwise identical results.
+ * Work schedules (HGEMM_OPT_SCHEDULE).  Dense kernels: both cut the same
+ * work into the same work ids (hgemm_plan_t: sk_ranges stream-K ranges, then
+ * dp_tiles whole tiles) and give bitwise identical results.  Split-K: the
+ * static schedule gives each CTA one equal range of units; the dynamic one
+ * keeps about 3/4 of the units in one range per SM and cuts the rest into
+ * small chunks that the SMs that finish first take over (results are
+ * deterministic for each schedule; the two differ in fp32 summation order).
  *   STATIC (default): plan->grid / cta_group persistent clusters; cluster c
  *     takes ids c, c + P, c + 2P, ... (P clusters).
  *   DYNAMIC: plan->work_ids clusters are launched, one per id; a cluster that
@@ -232,6 +236,11 @@ typedef struct {
   int64_t sk_units;      /* dense: (num_tiles - dp_tiles) * k_blocks, cut evenly over clusters */
   int32_t sk_ranges;     /* dense: stream-K ranges, work ids [0, sk_ranges); 0 without stream-K */
   int32_t work_ids;      /* dense: sk_ranges + dp_tiles; ids >= sk_ranges are whole tiles  */
+  int32_t schedule;      /* hgemm_schedule_t the plan was made for                         */
+  int32_t splitk_chunks; /* split-K: work ids (chunks of units); = grid under STATIC         */
+  int64_t splitk_head_units; /* split-K: units in chunks [0, grid) (all of them under STATIC;
+                                under DYNAMIC about 3/4, the rest in splitk_chunks - grid
+                                small chunks)                                             */
 } hgemm_plan_t;
 
 /*
@@ -244,6 +253,11 @@ typedef struct {
 hgemm_status_t hgemm_plan(int64_t M, int64_t N, int64_t K, hgemm_layout_t layout, hgemm_dtype_t in_dtype,
                           hgemm_dtype_t acc_dtype, hgemm_dtype_t out_dtype, int32_t num_sms, int32_t variant,
                           int32_t group_m, int32_t stream_k, hgemm_plan_t* plan);
+
+/* hgemm_plan for a given hgemm_schedule_t (hgemm_plan plans for STATIC). */
+hgemm_status_t hgemm_plan_ex(int64_t M, int64_t N, int64_t K, hgemm_layout_t layout, hgemm_dtype_t in_dtype,
+                             hgemm_dtype_t acc_dtype, hgemm_dtype_t out_dtype, int32_t num_sms, int32_t variant,
+                             int32_t group_m, int32_t stream_k, int32_t schedule, hgemm_plan_t* plan);
 
 /*
  * hgemm_plan_work_item -- the index-th item of cluster `cluster`'s work list
@@ -274,10 +288,13 @@ hgemm_status_t hgemm_plan_tile(const hgemm_plan_t* plan, int32_t t, int32_t* til
 
 /*
  * hgemm_plan_splitk_range -- for a split-K plan, the contiguous range of
- * (tile, k-block) work units that CTA `cta` owns: units [*begin, *end) of the
- * tile-major linear order (unit u = tile * k_blocks + kb).
+ * (tile, k-block) work units in chunk `chunk` (0 <= chunk <
+ * plan->splitk_chunks): units [*begin, *end) of the tile-major linear order
+ * (unit u = tile * k_blocks + kb).  Under STATIC chunk c is CTA c's range;
+ * under DYNAMIC the first plan->grid chunks start on the CTAs that run first
+ * and the small chunks after them go to whichever CTA finishes first.
  */
-hgemm_status_t hgemm_plan_splitk_range(const hgemm_plan_t* plan, int32_t cta, int64_t* begin, int64_t* end);
+hgemm_status_t hgemm_plan_splitk_range(const hgemm_plan_t* plan, int32_t chunk, int64_t* begin, int64_t* end);
 
 /*
  * hgemm_encode_idesc -- the 32-bit tcgen05.mma instruction descriptor the

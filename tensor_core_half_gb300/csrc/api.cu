@@ -184,8 +184,10 @@ void fill_dense_plan(DenseKind kind, const DenseChoice& ch, int64_t M, int64_t N
 
 hgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int layout, int in, int acc, int out, int num_sms,
                          int smem_optin, const int capacity_in[kNumDenseKinds], int variant, int group_m, int max_ctas,
-                         bool allow_sk, hgemm_plan_t* p) {
+                         bool allow_sk, int schedule, hgemm_plan_t* p) {
   memset(p, 0, sizeof(*p));
+  if (schedule != HGEMM_SCHEDULE_STATIC && schedule != HGEMM_SCHEDULE_DYNAMIC) return HGEMM_ERR_INVALID_ARG;
+  p->schedule = schedule;
   hgemm_status_t st = check_problem(M, N, K, layout, in, acc, out);
   if (st != HGEMM_OK) return st;
   if (num_sms <= 0) return HGEMM_ERR_INVALID_ARG;
@@ -222,7 +224,10 @@ hgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int layout, int in, in
     p->group_m = 1;
     p->smem_bytes = splitk_smem_bytes(mma_n, p->stages);
     p->tmem_cols = splitk_tmem_cols(mma_n);
-    p->workspace_bytes = (int64_t)splitk_workspace_bytes(p->grid, mma_n, p->num_tiles);
+    const SplitChunks ch = splitk_chunks(units, p->grid, schedule == HGEMM_SCHEDULE_DYNAMIC);
+    p->splitk_chunks = (int32_t)ch.count();
+    p->splitk_head_units = ch.head;
+    p->workspace_bytes = (int64_t)splitk_workspace_bytes(ch.count(), mma_n, p->num_tiles);
     return HGEMM_OK;
   }
   DenseKind kind = kDense2Sm256;
@@ -329,12 +334,19 @@ uint64_t hgemm_encode_smem_desc(uint32_t smem_addr, uint32_t lbo_bytes, uint32_t
   return make_smem_desc(smem_addr, lbo_bytes, sbo_bytes, swizzle_mode);
 }
 
+hgemm_status_t hgemm_plan_ex(int64_t M, int64_t N, int64_t K, hgemm_layout_t layout, hgemm_dtype_t in_dtype,
+                             hgemm_dtype_t acc_dtype, hgemm_dtype_t out_dtype, int32_t num_sms, int32_t variant,
+                             int32_t group_m, int32_t stream_k, int32_t schedule, hgemm_plan_t* plan) {
+  if (!plan || group_m < 0 || stream_k < 0 || stream_k > 1) return HGEMM_ERR_INVALID_ARG;
+  return make_plan(M, N, K, layout, in_dtype, acc_dtype, out_dtype, num_sms, kDefaultSmemOptin, nullptr, variant,
+                   group_m, 0, stream_k != 0, schedule, plan);
+}
+
 hgemm_status_t hgemm_plan(int64_t M, int64_t N, int64_t K, hgemm_layout_t layout, hgemm_dtype_t in_dtype,
                           hgemm_dtype_t acc_dtype, hgemm_dtype_t out_dtype, int32_t num_sms, int32_t variant,
                           int32_t group_m, int32_t stream_k, hgemm_plan_t* plan) {
-  if (!plan || group_m < 0 || stream_k < 0 || stream_k > 1) return HGEMM_ERR_INVALID_ARG;
-  return make_plan(M, N, K, layout, in_dtype, acc_dtype, out_dtype, num_sms, kDefaultSmemOptin, nullptr, variant,
-                   group_m, 0, stream_k != 0, plan);
+  return hgemm_plan_ex(M, N, K, layout, in_dtype, acc_dtype, out_dtype, num_sms, variant, group_m, stream_k,
+                       HGEMM_SCHEDULE_STATIC, plan);
 }
 
 hgemm_status_t hgemm_plan_work_item(const hgemm_plan_t* plan, int32_t cluster, int32_t index, int32_t* tile,
@@ -382,12 +394,16 @@ hgemm_status_t hgemm_plan_tile(const hgemm_plan_t* plan, int32_t t, int32_t* til
   return HGEMM_OK;
 }
 
-hgemm_status_t hgemm_plan_splitk_range(const hgemm_plan_t* plan, int32_t cta, int64_t* begin, int64_t* end) {
-  if (!plan || !begin || !end || plan->variant != HGEMM_VARIANT_SPLITK || cta < 0 || cta >= plan->grid)
+hgemm_status_t hgemm_plan_splitk_range(const hgemm_plan_t* plan, int32_t chunk, int64_t* begin, int64_t* end) {
+  if (!plan || !begin || !end || plan->variant != HGEMM_VARIANT_SPLITK || chunk < 0 || chunk >= plan->splitk_chunks)
     return HGEMM_ERR_INVALID_ARG;
-  const int64_t units = (int64_t)plan->num_tiles * plan->k_blocks;
-  *begin = splitk_begin(cta, units, plan->grid);
-  *end = splitk_begin((int64_t)cta + 1, units, plan->grid);
+  SplitChunks ch;
+  ch.units = (int64_t)plan->num_tiles * plan->k_blocks;
+  ch.head = plan->splitk_head_units;
+  ch.big = plan->grid;
+  ch.n_small = plan->splitk_chunks - plan->grid;
+  *begin = ch.begin(chunk);
+  *end = ch.begin((int64_t)chunk + 1);
   return HGEMM_OK;
 }
 
@@ -538,7 +554,7 @@ hgemm_status_t hgemm_run(hgemm_handle_t h, const void* A, const void* B, void* C
 
   hgemm_plan_t p;
   st = make_plan(M, N, K, layout, in_dtype, acc_dtype, out_dtype, h->sm_count, h->smem_optin, h->capacity,
-                 h->force_variant, h->group_m, h->max_ctas, h->stream_k, &p);
+                 h->force_variant, h->group_m, h->max_ctas, h->stream_k, h->schedule, &p);
   if (st != HGEMM_OK) return st;
 
   if (p.variant == HGEMM_VARIANT_SPLITK) {
@@ -547,8 +563,8 @@ hgemm_status_t hgemm_run(hgemm_handle_t h, const void* A, const void* B, void* C
     if (!encode_2d(&tmW, in_dtype, B, (uint64_t)K, (uint64_t)N, 64, 128) ||
         !encode_2d(&tmX, in_dtype, A, (uint64_t)K, (uint64_t)M, 64, (uint32_t)mma_n))
       return HGEMM_ERR_CUDA;
-    const size_t partial_bytes = (size_t)p.grid * 2 * 128 * (size_t)mma_n * sizeof(float);
-    st = ensure_workspace(h, partial_bytes, (size_t)p.num_tiles * 2, s);  // arrivals, publications
+    const size_t partial_bytes = (size_t)p.splitk_chunks * 2 * 128 * (size_t)mma_n * sizeof(float);
+    st = ensure_workspace(h, partial_bytes, (size_t)p.num_tiles * 2, s);  // one arrival counter per tile, spare
     if (st != HGEMM_OK) return st;
     if (p.smem_bytes > h->splitk_prepared_smem) return HGEMM_ERR_UNSUPPORTED;
     SplitKArgs args;
@@ -559,6 +575,10 @@ hgemm_status_t hgemm_run(hgemm_handle_t h, const void* A, const void* B, void* C
     args.n_tiles = p.num_tiles;
     args.k_blocks = p.k_blocks;
     args.units = (int64_t)p.num_tiles * p.k_blocks;
+    args.head = p.splitk_head_units;
+    args.big = p.grid;
+    args.n_small = p.splitk_chunks - p.grid;
+    args.dynamic = h->schedule == HGEMM_SCHEDULE_DYNAMIC ? 1 : 0;
     args.stages = p.stages;
     args.idesc = make_idesc(128, mma_n, in_dtype == HGEMM_BF16, true, false, false);
     args.out_bf16 = out_dtype == HGEMM_BF16;
@@ -569,7 +589,8 @@ hgemm_status_t hgemm_run(hgemm_handle_t h, const void* A, const void* B, void* C
     args.tickets = h->tickets;
     args.C = C;
     args.trace = h->trace;
-    return cuda_status(splitk_launch(tmW, tmX, args, p.grid, p.smem_bytes, s));
+    // Dynamic schedule: one CTA per chunk; the CTAs that run take over the rest.
+    return cuda_status(splitk_launch(tmW, tmX, args, args.dynamic ? p.splitk_chunks : p.grid, p.smem_bytes, s));
   }
 
   const DenseKind kind = kind_of(p.variant);

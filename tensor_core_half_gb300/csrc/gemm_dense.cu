@@ -27,6 +27,7 @@
 //   warps 2..5  epilogue; warp w reads TMEM lanes 32*(w%4) .. 32*(w%4)+31
 #include <cuda_fp16.h>
 
+#include "clc.cuh"
 #include "desc.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
@@ -78,46 +79,23 @@ __device__ __forceinline__ uint32_t f16x2_to_out(uint32_t h2, bool out_bf16) {
 
 // The work ids one role walks through.  Static schedule: the cluster's fixed
 // walk.  Dynamic schedule: the cluster's own id, then ids taken over from
-// clusters that have not started, by cluster launch control ("Persistent
-// kernel" section of the tcgen05 walkthrough: the page names dynamic
-// scheduling as the next step after its static scheduler).  One thread of the
-// pair (the issuer) asks for the next id as soon as it starts an id; every
-// role reads each response from its own shared memory and then arrives on
-// the slot's empty barrier in CTA 0, so the slot can take the next request.
+// clusters that have not started (ClcIds, cluster launch control).
 template <int CG, int SLOTS>
 struct IdFeed {
   WorkIter it;
+  ClcIds<CG, SLOTS> clc;
   int32_t cluster, nclusters;
-  bool dynamic, issuer, warp_wide, arrive;
+  bool dynamic;
   bool started = false, finished = false;
-  int32_t taken = 0;      // responses read
-  int32_t requested = 0;  // requests issued (issuer only)
-  uint32_t resp0, full0, empty0;  // slot 0 addresses in this CTA
+  bool want = false;  // issuer: the current id's request is still to be made
 
-  __device__ IdFeed(const DenseArgs& a, int32_t cluster_, int32_t nclusters_, uint32_t resp0_, uint32_t full0_,
-                    uint32_t empty0_, bool issuer_, bool warp_wide_, bool arrive_)
+  __device__ IdFeed(const DenseArgs& a, int32_t cluster_, int32_t nclusters_, uint32_t resp0, uint32_t full0,
+                    uint32_t empty0, bool issuer, bool warp_wide, bool arrive)
       : it(a.sk_ranges, a.dp_tiles, a.sk_units, a.k_blocks),
+        clc(resp0, full0, empty0, issuer, warp_wide, arrive),
         cluster(cluster_),
         nclusters(nclusters_),
-        dynamic(a.dynamic != 0),
-        issuer(issuer_),
-        warp_wide(warp_wide_),
-        arrive(arrive_),
-        resp0(resp0_),
-        full0(full0_),
-        empty0(empty0_) {}
-
-  __device__ bool request(const WaitCtl& ctl) {
-    const int32_t r = requested;  // 0-based request number
-    const uint32_t slot = (uint32_t)(r % SLOTS);
-    if (!mbar_wait<CG == 2>(empty0 + 8u * slot, (uint32_t)(((r / SLOTS) & 1) ^ 1), ctl)) return false;
-    const uint32_t fb = full0 + 8u * slot;
-    mbar_arrive_expect_tx(fb, 16);
-    if constexpr (CG == 2) mbar_arrive_expect_tx_cluster(mapa_shared(fb, 1), 16);
-    clc_try_cancel<CG>(resp0 + 16u * slot, fb);
-    ++requested;
-    return true;
-  }
+        dynamic(a.dynamic != 0) {}
 
   // 1: an item in w; 0: no work left; -1: a wait gave up.
   __device__ int next(WorkItem& w, const WaitCtl& ctl) {
@@ -129,42 +107,37 @@ struct IdFeed {
           it.start_static(cluster, nclusters);
         } else {
           it.start(cluster);
-          if (issuer && !request(ctl)) return -1;
+          want = clc.issuer;
         }
       }
       if (!dynamic) return it.next_static(w) ? 1 : 0;
       if (it.next_in_id(w)) return 1;
-      const int32_t r = taken;  // 0-based response number
-      const uint32_t slot = (uint32_t)(r % SLOTS);
-      if (!mbar_wait<CG == 2>(full0 + 8u * slot, (uint32_t)((r / SLOTS) & 1), ctl)) return -1;
-      const int32_t x = clc_first_ctaid_x(resp0 + 16u * slot);
-      ++taken;
-      if (warp_wide) __syncwarp();
-      if (arrive) {
-        if constexpr (CG == 1)
-          mbar_arrive(empty0 + 8u * slot);
-        else
-          mbar_arrive_cluster(mapa_shared(empty0 + 8u * slot, 0));
+      if (want) {  // an id shorter than the lead: ask now
+        want = false;
+        if (!clc.request(ctl)) return -1;
       }
-      if (x < 0) {
+      int64_t id = 0;
+      const int got = clc.fetch(&id, ctl);
+      if (got < 0) return -1;
+      if (got == 0) {
         finished = true;
         started = false;
         return 0;
       }
-      it.start(x / CG);
-      if (issuer && !request(ctl)) return -1;
+      it.start(id);
+      want = clc.issuer;
     }
   }
 
-  // After giving up: wait for the response of a request this thread issued
-  // and did not read, so that nothing lands in shared memory after exit.
-  __device__ bool drain(const WaitCtl& ctl) {
-    for (int32_t r = taken; r < requested; ++r) {
-      const uint32_t slot = (uint32_t)(r % SLOTS);
-      if (!mbar_wait<CG == 2>(full0 + 8u * slot, (uint32_t)((r / SLOTS) & 1), ctl)) return false;
-    }
-    return true;
+  // Issuer, after loading a k-block of the current item: `left` k-blocks of
+  // the item remain; ask for the next id when clc_time_to_ask says so.
+  __device__ bool poll(int64_t left, const WaitCtl& ctl) {
+    if (!want || !clc_time_to_ask(left + it.left_after_item(), it.id_length())) return true;
+    want = false;
+    return clc.request(ctl);
   }
+
+  __device__ bool drain(const WaitCtl& ctl) { return clc.drain(ctl); }
 };
 
 template <int CG, int BN, int STAGES>
@@ -214,12 +187,9 @@ __global__ void __launch_bounds__(192, 1)
         mbar_init(tempty_bar(b), 4 * CG);  // every epilogue warp of the pair arrives
       }
       mbar_init(drain_bar, 1);
-      for (int i = 0; i < S::CLC_SLOTS; ++i) {
-        mbar_init(clc_full0 + 8u * i, 1);
-        // readers of every response: producer, MMA issuer and 4 epilogue warps
-        // of CTA 0, producer and 4 epilogue warps of CTA 1
-        mbar_init(clc_empty0 + 8u * i, CG == 2 ? 11 : 6);
-      }
+      // readers of every response: producer, MMA issuer and 4 epilogue warps
+      // of CTA 0, producer and 4 epilogue warps of CTA 1
+      ClcIds<CG, S::CLC_SLOTS>::init(clc_full0, clc_empty0, CG == 2 ? 11 : 6);
       *abort_flag = 0u;
       fence_mbar_init();
       prefetch_tmap(&tmA);
@@ -303,6 +273,10 @@ __global__ void __launch_bounds__(192, 1)
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
+          }
+          if (!feed.poll(w.kb1 - kb - 1, ctl)) {
+            ok = false;
+            break;
           }
         }
         trace_event(tb, kRoleProducer, kTraceStall, w.tile, (int32_t)stall);

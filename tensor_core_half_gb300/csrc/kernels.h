@@ -87,14 +87,18 @@ struct SplitKArgs {
   int32_t n_tiles;   // ceil(N / 128)
   int32_t k_blocks;  // ceil(K / 64)
   int64_t units;     // n_tiles * k_blocks
+  int64_t head;      // units covered by the first `big` chunks (all units under the static schedule)
+  int32_t big;       // big chunks (= CTAs of the static schedule)
+  int32_t n_small;   // small chunks after them (dynamic schedule), else 0
+  int32_t dynamic;   // 1: one CTA per chunk, chunks taken over by cluster launch control
   int32_t stages;
   uint32_t idesc;
   int32_t out_bf16;
   int32_t inject;
   uint64_t timeout_ns;
   int32_t* status;
-  float* partials;   // [grid][2][128][mma_n] fp32
-  int32_t* tickets;  // [2][n_tiles] arrivals, publications; all zero between launches
+  float* partials;   // [big + n_small chunks][2][128][mma_n] fp32
+  int32_t* tickets;  // [n_tiles] arrival counters (space for 2 x n_tiles); all zero between launches
   void* C;           // [M][N] row-major
   TraceBuf* trace;   // null unless tracing
 };
@@ -104,7 +108,7 @@ int splitk_stage_bytes(int mma_n);
 int splitk_smem_bytes(int mma_n, int stages);
 int splitk_stages_for(int mma_n, int smem_optin);
 int splitk_tmem_cols(int mma_n);
-size_t splitk_workspace_bytes(int grid, int mma_n, int n_tiles);
+size_t splitk_workspace_bytes(int64_t chunks, int mma_n, int n_tiles);
 cudaError_t splitk_prepare(int smem_bytes);
 cudaError_t splitk_launch(const CUtensorMap& tmW, const CUtensorMap& tmX, const SplitKArgs& args, int grid,
                           int smem_bytes, cudaStream_t stream);

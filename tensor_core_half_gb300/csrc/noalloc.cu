@@ -172,6 +172,10 @@ extern "C" hgemm_status_t hgemm_run_splitk_noalloc(const void* A, const void* B,
   args.n_tiles = (int32_t)n_tiles;
   args.k_blocks = (int32_t)k_blocks;
   args.units = units;
+  args.head = units;  // the static split: one equal range per CTA
+  args.big = (int32_t)grid;
+  args.n_small = 0;
+  args.dynamic = 0;
   args.stages = stages;
   args.idesc = hg::make_idesc(128, mma_n, in_dtype == HGEMM_BF16, true, false, false);
   args.out_bf16 = out_dtype == HGEMM_BF16;

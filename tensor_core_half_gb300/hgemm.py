@@ -78,7 +78,8 @@ class hgemm_plan_t(ctypes.Structure):
         "variant", "cta_group", "tile_m", "tile_n", "block_k", "stages", "tiles_m", "tiles_n", "num_tiles",
         "k_blocks", "grid", "group_m", "smem_bytes", "tmem_cols")] + [
         ("workspace_bytes", ctypes.c_int64), ("dp_tiles", ctypes.c_int32), ("stream_k", ctypes.c_int32),
-        ("sk_units", ctypes.c_int64), ("sk_ranges", ctypes.c_int32), ("work_ids", ctypes.c_int32)]
+        ("sk_units", ctypes.c_int64), ("sk_ranges", ctypes.c_int32), ("work_ids", ctypes.c_int32),
+        ("schedule", ctypes.c_int32), ("splitk_chunks", ctypes.c_int32), ("splitk_head_units", ctypes.c_int64)]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -104,6 +105,9 @@ _lib.hgemm_set_option.restype = _i32
 _lib.hgemm_set_option.argtypes = [_vp, _i32, _i64]
 _lib.hgemm_status_string.restype = ctypes.c_char_p
 _lib.hgemm_status_string.argtypes = [_i32]
+_lib.hgemm_plan_ex.restype = _i32
+_lib.hgemm_plan_ex.argtypes = [_i64, _i64, _i64, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
+                               ctypes.POINTER(hgemm_plan_t)]
 _lib.hgemm_plan.restype = _i32
 _lib.hgemm_plan.argtypes = [_i64, _i64, _i64, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
                             ctypes.POINTER(hgemm_plan_t)]
@@ -201,10 +205,16 @@ def hgemm_set_option(h, option, value) -> int:
 
 
 def hgemm_plan(M, N, K, layout=HGEMM_LAYOUT_TN, in_dtype=HGEMM_BF16, acc_dtype=HGEMM_F32, out_dtype=HGEMM_BF16,
-               num_sms=152, variant=HGEMM_VARIANT_AUTO, group_m=0, stream_k=1):
+               num_sms=152, variant=HGEMM_VARIANT_AUTO, group_m=0, stream_k=1, schedule=None):
+    """hgemm_plan, or hgemm_plan_ex when a schedule is given."""
     p = hgemm_plan_t()
-    st = _lib.hgemm_plan(int(M), int(N), int(K), int(layout), int(in_dtype), int(acc_dtype), int(out_dtype),
-                         int(num_sms), int(variant), int(group_m), int(stream_k), ctypes.byref(p))
+    if schedule is None:
+        st = _lib.hgemm_plan(int(M), int(N), int(K), int(layout), int(in_dtype), int(acc_dtype), int(out_dtype),
+                             int(num_sms), int(variant), int(group_m), int(stream_k), ctypes.byref(p))
+    else:
+        st = _lib.hgemm_plan_ex(int(M), int(N), int(K), int(layout), int(in_dtype), int(acc_dtype), int(out_dtype),
+                                int(num_sms), int(variant), int(group_m), int(stream_k), int(schedule),
+                                ctypes.byref(p))
     return int(st), p
 
 

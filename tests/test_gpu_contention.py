@@ -58,6 +58,39 @@ def _timed(h, A, B, C, launches, load, busy, bg):
 
 
 @pytest.mark.parametrize("schedule", ["static", "dynamic"])
+def test_splitk_parity_with_busy_sms(load, schedule):
+    M, N, K = 16, 16384, 4096
+    a, b, ab, bb = parity.inputs(M, N, K, "TN", "bf16", ("normal", 1.0), 92)
+    A, B = a.cuda(), b.cuda()
+    C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    bg = torch.cuda.Stream()
+    with hgemm.Handle() as h:
+        h.set_option(hgemm.HGEMM_OPT_SCHEDULE, hgemm.SCHEDULES[schedule])
+        _timed(h, A, B, C, 5, load, 24, bg)
+    parity.check(workloads.bits(C.cpu()), ab, bb, M, N, K, "TN", "bf16", "f32", "bf16")
+
+
+def test_splitk_rates_with_busy_sms(load):
+    # Reported (run with -s), and the dynamic schedule must not lose to the
+    # static one once SMs are busy.
+    M, N, K = 16, 16384, 8192
+    A = torch.randn((M, K), device="cuda").bfloat16()
+    B = torch.randn((N, K), device="cuda").bfloat16()
+    C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    bg = torch.cuda.Stream()
+    rate = {}
+    for busy in (0, 16):
+        for schedule in ("static", "dynamic"):
+            with hgemm.Handle() as h:
+                h.set_option(hgemm.HGEMM_OPT_SCHEDULE, hgemm.SCHEDULES[schedule])
+                ms = _timed(h, A, B, C, 50, load, busy, bg)
+            rate[(busy, schedule)] = (M * K + N * K + M * N) * 2 / ms / 1e6
+            print("16x16384x8192 bf16 split-K, %2d SMs held by other work, %-7s schedule: %.0f GB/s" % (
+                busy, schedule, rate[(busy, schedule)]))
+    assert rate[(16, "dynamic")] > rate[(16, "static")]
+
+
+@pytest.mark.parametrize("schedule", ["static", "dynamic"])
 @pytest.mark.parametrize("sk", [1, 0])
 def test_parity_with_busy_sms(load, schedule, sk):
     M, N, K = 2048, 4096, 1024

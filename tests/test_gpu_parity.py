@@ -127,6 +127,26 @@ def test_splitk_shapes(h, M, N, K):
     parity.check(got, ab, bb, M, N, K, "TN", "bf16", "f32", "bf16")
 
 
+@pytest.mark.parametrize("M", [1, 16, 33, 64])
+@pytest.mark.parametrize("N,K", [(4096, 1024), (384, 8192), (16384, 2048), (1000, 4104)])
+def test_splitk_dynamic_parity(h, M, N, K):
+    # Dynamic split-K: big chunks on the SMs that start, small chunks taken
+    # over by those that finish first; fixed summation order per tile.
+    a, b, ab, bb = parity.inputs(M, N, K, "TN", "bf16", ("normal", 1.0), 86)
+    got = run(h, a, b, M, N, K, "TN", "f32", "bf16", "splitk", schedule="dynamic")
+    parity.check(got, ab, bb, M, N, K, "TN", "bf16", "f32", "bf16")
+    again = run(h, a, b, M, N, K, "TN", "f32", "bf16", "splitk", schedule="dynamic")
+    assert np.array_equal(got, again)
+
+
+def test_splitk_dynamic_small_integers_bit_exact(h):
+    M, N, K = 40, 8192, 4096
+    a, b, ab, bb = parity.inputs(M, N, K, "TN", "bf16", ("int", -4, 4), 87)
+    got = run(h, a, b, M, N, K, "TN", "f32", "bf16", "splitk", schedule="dynamic")
+    ref, _, _ = oracle.gemm(ab, bb, M, N, K, "TN", "bf16", "bf16")
+    assert np.array_equal(got, ref)
+
+
 def test_splitk_small_integers_bit_exact(h):
     M, N, K = 16, 2048, 4096
     a, b, ab, bb = parity.inputs(M, N, K, "TN", "f16", ("int", -4, 4), 23)
@@ -239,7 +259,7 @@ def test_direct_epilogue_parity(h, variant, layout, M, N, K, combo):
 
 
 @pytest.mark.parametrize("variant,M,N,K", [("2sm256", 300, 264, 200), ("1sm128", 130, 136, 72),
-                                           ("2sm192", 257, 392, 136)])
+                                           ("2sm192", 257, 392, 136), ("splitk", 17, 1000, 8192)])
 def test_direct_epilogue_guard_bands_untouched(h, variant, M, N, K):
     a, b, ab, bb = parity.inputs(M, N, K, "TN", "bf16", ("normal", 1.0), 85)
     pad = 4096
@@ -318,7 +338,7 @@ def test_argument_validation(h):
 
 @pytest.mark.parametrize("variant,M,schedule", [("1sm128", 512, "static"), ("2sm256", 512, "static"),
                                                 ("splitk", 16, "static"), ("1sm128", 4096, "dynamic"),
-                                                ("2sm256", 4096, "dynamic")])
+                                                ("2sm256", 4096, "dynamic"), ("splitk", 16, "dynamic")])
 def test_bounded_wait_gives_up_and_recovers(h, variant, M, schedule):
     # The first CTA's producer drops its first stage; the MMA warp's wait on that
     # stage can never succeed, gives up after the limit, and every role exits.

@@ -107,3 +107,31 @@ def test_dynamic_schedule_takes_over_pending_clusters(variant, M, N, K, sk):
         if sp["role"] == "mma":
             got[(sp["tile"], sp["begin_value"], sp["end_value"])] += 1
     assert got == expect
+
+
+def test_dynamic_splitk_takes_over_small_chunks():
+    """Dynamic split-K: one CTA is launched per chunk, the CTAs that run
+    first take over the small chunks, and every (tile, k-block) unit is
+    multiplied exactly once."""
+    M, N, K = 16, 16384, 4096
+    with hgemm.Handle() as h:
+        h.set_option(hgemm.HGEMM_OPT_SCHEDULE, hgemm.HGEMM_SCHEDULE_DYNAMIC)
+        h.set_option(hgemm.HGEMM_OPT_TRACE, 1 << 18)
+        a, b, _, _ = parity.inputs(M, N, K, "TN", "bf16", ("normal", 1.0), 73)
+        A, B = a.cuda(), b.cuda()
+        C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        h.run(A, B, C, layout="TN", acc="f32")
+        assert h.sync_status()[0] == hgemm.HGEMM_OK
+        st, n, rows = hgemm.hgemm_trace_read(h.h, 1 << 18)
+        assert st == hgemm.HGEMM_OK and n == len(rows) > 0
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    st, p = hgemm.hgemm_plan(M, N, K, num_sms=sms, schedule=hgemm.HGEMM_SCHEDULE_DYNAMIC)
+    assert p.variant == hgemm.HGEMM_VARIANT_SPLITK and p.splitk_chunks > p.grid
+    began = {r[1] for r in rows if r[2] == 0 and r[3] == 1}
+    assert 0 < len(began) <= p.grid < p.splitk_chunks
+    covered = collections.Counter()
+    for sp in trace.spans(rows):
+        if sp["role"] == "mma":
+            for kb in range(sp["begin_value"], sp["end_value"]):
+                covered[(sp["tile"], kb)] += 1
+    assert len(covered) == p.num_tiles * p.k_blocks and set(covered.values()) == {1}

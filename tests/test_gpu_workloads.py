@@ -33,16 +33,18 @@ def _inputs(w):
     return _cache[key]
 
 
-def _check(h, w, variant="auto"):
+def _check(h, w, variant="auto", schedule="static"):
     a, b, ab, bb = _inputs(w)
     A, B = a.cuda(), b.cuda()
     C = torch.empty((w.M, w.N), dtype=TORCH_DT[w.out_dtype], device="cuda")
     h.set_option(hgemm.HGEMM_OPT_FORCE_VARIANT, hgemm.VARIANTS[variant])
+    h.set_option(hgemm.HGEMM_OPT_SCHEDULE, hgemm.SCHEDULES[schedule])
     try:
         h.run(A, B, C, layout=w.layout, acc=w.acc_dtype)
         st, detail = h.sync_status()
     finally:
         h.set_option(hgemm.HGEMM_OPT_FORCE_VARIANT, hgemm.HGEMM_VARIANT_AUTO)
+        h.set_option(hgemm.HGEMM_OPT_SCHEDULE, hgemm.HGEMM_SCHEDULE_STATIC)
     assert st == hgemm.HGEMM_OK, hex(detail)
     got = workloads.bits(C.cpu())
     del A, B, C
@@ -58,6 +60,11 @@ ORDER = sorted(workloads.WORKLOADS, key=lambda n: (workloads.WORKLOADS[n].M * wo
 @pytest.mark.parametrize("name", ORDER)
 def test_workload(h, name):
     _check(h, workloads.WORKLOADS[name])
+
+
+@pytest.mark.parametrize("name", ["skinny16x16384x8192_bf16", "ragged1000x3000x4104_bf16", "square4096_bf16"])
+def test_workload_dynamic_schedule(h, name):
+    _check(h, workloads.WORKLOADS[name], schedule="dynamic")
 
 
 @pytest.mark.parametrize("variant", ["1sm128", "1sm256"])

@@ -146,6 +146,37 @@ def test_splitk_partition(M, N, K, sms):
     assert H.hgemm_plan_splitk_range(p, p.grid)[0] == ST_INV
 
 
+@pytest.mark.parametrize("M,N,K,sms", [(16, 16384, 8192, 152), (1, 8, 64, 152), (64, 1000, 72, 148),
+                                       (33, 4096, 1024, 152), (16, 16384, 8192, 7), (8, 256, 16384, 152)])
+def test_splitk_dynamic_chunks(M, N, K, sms):
+    """Dynamic split-K chunks: the first `grid` chunks (one per SM) hold about
+    three quarters of the units, the small chunks (about a quarter of an SM's
+    share each) the rest; all of them together cover every unit once, in
+    order, and no chunk is empty."""
+    st, p = H.hgemm_plan(M, N, K, num_sms=sms, schedule=H.HGEMM_SCHEDULE_DYNAMIC)
+    assert st == ST_OK and p.variant == H.HGEMM_VARIANT_SPLITK and p.schedule == H.HGEMM_SCHEDULE_DYNAMIC
+    units = p.num_tiles * p.k_blocks
+    sizes, prev_end = [], 0
+    for g in range(p.splitk_chunks):
+        s, b, e = H.hgemm_plan_splitk_range(p, g)
+        assert s == ST_OK and b == prev_end and e > b
+        sizes.append(e - b)
+        prev_end = e
+    assert prev_end == units
+    assert H.hgemm_plan_splitk_range(p, p.splitk_chunks)[0] == ST_INV
+    big, small = sizes[:p.grid], sizes[p.grid:]
+    assert max(big) - min(big) <= 1
+    if units >= 4 * p.grid:
+        assert small and max(small) - min(small) <= 1 and max(small) < min(big)
+        assert sum(big) == p.splitk_head_units and abs(sum(small) - units // 4) <= 1
+        assert max(small) <= max(1, units // (p.grid * 4)) + 1
+    else:
+        assert not small and p.splitk_head_units == units  # too little work to split further
+    # the static plan of the same problem: one range per CTA
+    st, q = H.hgemm_plan(M, N, K, num_sms=sms, schedule=H.HGEMM_SCHEDULE_STATIC)
+    assert q.splitk_chunks == q.grid == p.grid and q.splitk_head_units == units
+
+
 # ------------------------------------------------------------ descriptors ----
 # Expected words are written out by hand from the field tables:
 #   idesc: D fmt bits 4-5 (f32 = 1), A fmt 7-9 / B fmt 10-12 (bf16 = 1),
