@@ -217,6 +217,7 @@ def main():
     ap.add_argument("--stream-k", type=int, default=1, choices=[0, 1])
     ap.add_argument("--schedule", default="static", choices=["static", "dynamic"])
     ap.add_argument("--epilogue", default="tma", choices=["tma", "direct"])
+    ap.add_argument("--group-m", type=int, default=0, help="rasterisation group height in tiles (0: default)")
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -253,10 +254,12 @@ def main():
     handle.set_option(hgemm.HGEMM_OPT_STREAM_K, args.stream_k)
     handle.set_option(hgemm.HGEMM_OPT_SCHEDULE, hgemm.SCHEDULES[args.schedule])
     handle.set_option(hgemm.HGEMM_OPT_EPILOGUE, hgemm.EPILOGUES[args.epilogue])
+    if args.group_m > 0:
+        handle.set_option(hgemm.HGEMM_OPT_GROUP_M, args.group_m)
     st, plan = hgemm.hgemm_plan(w.M, w.N, w.K, hgemm.LAYOUTS[w.layout], hgemm.DTYPES[w.in_dtype],
                                 hgemm.DTYPES[w.acc_dtype], hgemm.DTYPES[w.out_dtype],
                                 torch.cuda.get_device_properties(dev).multi_processor_count,
-                                hgemm.VARIANTS[args.variant], 0, args.stream_k)
+                                hgemm.VARIANTS[args.variant], args.group_m, args.stream_k)
     stream = torch.cuda.current_stream(dev)
     sp = stream.cuda_stream
     lay, fin, facc, fout = (hgemm.LAYOUTS[w.layout], hgemm.DTYPES[w.in_dtype], hgemm.DTYPES[w.acc_dtype],
@@ -385,7 +388,7 @@ def main():
         "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "layout": w.layout, "in": w.in_dtype,
                    "acc": w.acc_dtype, "out": w.out_dtype, "variant": list(hgemm.VARIANTS)[plan.variant],
                    "grid": plan.grid if args.schedule == "static" else plan.work_ids * plan.cta_group,
-                   "schedule": args.schedule, "epilogue": args.epilogue, "tile": [plan.tile_m, plan.tile_n], "stages": plan.stages,
+                   "schedule": args.schedule, "epilogue": args.epilogue, "group_m": plan.group_m, "tile": [plan.tile_m, plan.tile_n], "stages": plan.stages,
                    "stream_k": {"dp_tiles": plan.dp_tiles, "sk_units": plan.sk_units} if plan.stream_k else None,
                    "parallelism": "replicas" if world > 1 else "single",
                    "l2": "inputs rotate over %d copies (%.0f MiB > 2x L2)" % (copies, copies * (in_bytes + c_bytes) / 2**20),

@@ -705,9 +705,12 @@ hgemm_status_t hgemm_run_host(hgemm_handle_t h, const void* A, const void* B, vo
       (e = grow(&sg.C, &sg.c_cap, c_bytes)) != cudaSuccess)
     return e == cudaErrorMemoryAllocation ? HGEMM_ERR_OOM : cuda_status(e);
 
-  // Row chunks of A and C: at least 512 rows (whole 256-row tiles), at most 8.
-  int64_t rows = ((M + 7) / 8 + 255) / 256 * 256;
-  if (rows < 512) rows = 512;
+  // Row chunks of A and C: at least 1024 rows (whole 256-row tiles), at most
+  // 4.  A chunk's GEMM must run at least as fast as the link delivers the
+  // next chunk of A (about 840 TFLOPS at 4096 x 4096 and 205 GB/s); 512-row
+  // chunks do not (measured 297 TFLOPS end to end at 4096^3 vs 306 with 4).
+  int64_t rows = ((M + 3) / 4 + 255) / 256 * 256;
+  if (rows < 1024) rows = 1024;
   const int nch = (int)((M + rows - 1) / rows);
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
