@@ -46,15 +46,18 @@ THROTTLE_BITS = {  # nvidia-smi clocks_event_reasons bit masks
     0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
     0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
     0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
-KERNEL_SOURCES = ["tensor_core_half_gb300/csrc/gemm_dense.cu", "tensor_core_half_gb300/csrc/gemm_splitk.cu",
-                  "tensor_core_half_gb300/csrc/ptx.cuh", "tensor_core_half_gb300/csrc/desc.cuh",
-                  "tensor_core_half_gb300/csrc/sched.cuh", "tensor_core_half_gb300/csrc/kernels.h"]
+_SHARED_SOURCES = ["ptx.cuh", "desc.cuh", "sched.cuh", "kernels.h", "clc.cuh"]
+KERNEL_SOURCES = {  # the files each kernel is compiled from
+    "dense": ["gemm_dense.cu"] + _SHARED_SOURCES,
+    "splitk": ["gemm_splitk.cu"] + _SHARED_SOURCES,
+}
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(kernel: str) -> str:
+    """Hash of one kernel's sources: stored ncu traffic is valid only while it matches."""
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as f:
+    for rel in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "tensor_core_half_gb300", "csrc", rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
@@ -76,7 +79,8 @@ def load_traffic(workload: str, variant: int):
     with open(p) as f:
         d = json.load(f)
     e = d.get("%s/%d" % (workload, variant))
-    if not e or e.get("kernel_hash") != kernel_source_hash():
+    kernel = "splitk" if variant == 4 else "dense"
+    if not e or e.get("kernel_hash") != kernel_source_hash(kernel):
         return None
     return e.get("dram_bytes_per_launch")
 
