@@ -218,7 +218,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=None)
     ap.add_argument("--variant", default="auto")
-    ap.add_argument("--stream-k", type=int, default=1, choices=[0, 1])
+    ap.add_argument("--stream-k", type=int, default=1, choices=[0, 1, 2])
     ap.add_argument("--schedule", default="static", choices=["static", "dynamic"])
     ap.add_argument("--epilogue", default="tma", choices=["tma", "direct"])
     ap.add_argument("--group-m", type=int, default=0, help="rasterisation group height in tiles (0: default)")

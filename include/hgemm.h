@@ -72,7 +72,9 @@ typedef enum {
   HGEMM_OPT_GROUP_M = 4,       /* value: rasterisation group height in tiles (default 8)      */
   HGEMM_OPT_MAX_CTAS = 5,      /* value: cap on persistent CTAs (0 = one per SM)              */
   HGEMM_OPT_STREAM_K = 6,      /* value: 1 (default) lets the planner split the last wave of
-                                  dense tiles along K (stream-K); 0 keeps every tile whole    */
+                                  dense tiles along K (stream-K) when its estimate favours it;
+                                  0 keeps every tile whole; 2 splits whenever the tile count
+                                  leaves a partial wave                                      */
   HGEMM_OPT_TRACE = 7,         /* value: capacity in events of a device trace buffer that the
                                   kernels append to (0 = off, the default); hgemm_trace_read */
   HGEMM_OPT_SCHEDULE = 8,      /* value: an hgemm_schedule_t for the dense kernels           */
@@ -247,7 +249,8 @@ typedef struct {
  * hgemm_plan -- the launch plan hgemm_run would use for these arguments on a
  * GPU with `num_sms` SMs (cluster capacity assumed num_sms / 2 pairs).
  * `variant` = HGEMM_VARIANT_AUTO or a forced variant; group_m = 0 for the
- * default; stream_k = 1 to allow stream-K, 0 to forbid it.  Validates the
+ * default; stream_k = 1 to allow stream-K, 0 to forbid it, 2 to force it
+ * (as HGEMM_OPT_STREAM_K).  Validates the
  * sizes, dtypes and layout like hgemm_run (pointers are not involved).
  */
 hgemm_status_t hgemm_plan(int64_t M, int64_t N, int64_t K, hgemm_layout_t layout, hgemm_dtype_t in_dtype,

@@ -46,7 +46,7 @@ struct Ctx {
   int inject = 0;
   int group_m = kDefaultGroupM;
   int max_ctas = 0;
-  bool stream_k = true;
+  int stream_k = 1;  // 0 never, 1 when the estimate says so, 2 whenever the tile count leaves a partial wave
   int schedule = HGEMM_SCHEDULE_STATIC;
   int epilogue = HGEMM_EPILOGUE_TMA_STORE;
   TraceBuf* trace = nullptr;  // device trace buffer (HGEMM_OPT_TRACE)
@@ -131,7 +131,7 @@ struct DenseChoice {
 // k-blocks of mainloop time per cluster (measured on GB300 with the kernel's
 // event trace: publishing or reducing a 256 x 256 fp32 partial).
 DenseChoice dense_choice(DenseKind kind, int64_t M, int64_t N, int64_t K, int capacity, int max_ctas,
-                         bool allow_sk) {
+                         int allow_sk) {
   const DenseKindInfo info = dense_kind_info(kind);
   const int64_t tiles = cdiv(M, 128 * info.cta_group) * cdiv(N, info.block_n);
   const int64_t kb = cdiv(K, 64);
@@ -146,7 +146,7 @@ DenseChoice dense_choice(DenseKind kind, int64_t M, int64_t N, int64_t K, int ca
     sk.sk_units = (tiles - sk.dp_tiles) * kb;
     sk.clusters = (int)std::min<int64_t>(P, sk.sk_units);
     sk.cost = (double)tiles / (double)sk.clusters + 30.0 / (double)kb;
-    if (sk.cost < dp.cost) best = sk;
+    if (sk.cost < dp.cost || allow_sk == 2) best = sk;
   }
   // relative mainloop efficiency per tile area (2-SM 256-wide tiles are the reference)
   const double eff = (kind == kDense2Sm256) ? 1.0 : (kind == kDense2Sm192 ? 0.78 : (kind == kDense1Sm256 ? 0.85 : 0.70));
@@ -184,7 +184,7 @@ void fill_dense_plan(DenseKind kind, const DenseChoice& ch, int64_t M, int64_t N
 
 hgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int layout, int in, int acc, int out, int num_sms,
                          int smem_optin, const int capacity_in[kNumDenseKinds], int variant, int group_m, int max_ctas,
-                         bool allow_sk, int schedule, hgemm_plan_t* p) {
+                         int allow_sk, int schedule, hgemm_plan_t* p) {
   memset(p, 0, sizeof(*p));
   if (schedule != HGEMM_SCHEDULE_STATIC && schedule != HGEMM_SCHEDULE_DYNAMIC) return HGEMM_ERR_INVALID_ARG;
   p->schedule = schedule;
@@ -337,9 +337,9 @@ uint64_t hgemm_encode_smem_desc(uint32_t smem_addr, uint32_t lbo_bytes, uint32_t
 hgemm_status_t hgemm_plan_ex(int64_t M, int64_t N, int64_t K, hgemm_layout_t layout, hgemm_dtype_t in_dtype,
                              hgemm_dtype_t acc_dtype, hgemm_dtype_t out_dtype, int32_t num_sms, int32_t variant,
                              int32_t group_m, int32_t stream_k, int32_t schedule, hgemm_plan_t* plan) {
-  if (!plan || group_m < 0 || stream_k < 0 || stream_k > 1) return HGEMM_ERR_INVALID_ARG;
+  if (!plan || group_m < 0 || stream_k < 0 || stream_k > 2) return HGEMM_ERR_INVALID_ARG;
   return make_plan(M, N, K, layout, in_dtype, acc_dtype, out_dtype, num_sms, kDefaultSmemOptin, nullptr, variant,
-                   group_m, 0, stream_k != 0, schedule, plan);
+                   group_m, 0, stream_k, schedule, plan);
 }
 
 hgemm_status_t hgemm_plan(int64_t M, int64_t N, int64_t K, hgemm_layout_t layout, hgemm_dtype_t in_dtype,
@@ -501,8 +501,8 @@ hgemm_status_t hgemm_set_option(hgemm_handle_t h, int32_t option, int64_t value)
       h->max_ctas = (int)value;
       return HGEMM_OK;
     case HGEMM_OPT_STREAM_K:
-      if (value < 0 || value > 1) return HGEMM_ERR_INVALID_ARG;
-      h->stream_k = value != 0;
+      if (value < 0 || value > 2) return HGEMM_ERR_INVALID_ARG;
+      h->stream_k = (int)value;
       return HGEMM_OK;
     case HGEMM_OPT_SCHEDULE:
       if (value != HGEMM_SCHEDULE_STATIC && value != HGEMM_SCHEDULE_DYNAMIC) return HGEMM_ERR_INVALID_ARG;

@@ -335,6 +335,19 @@ def test_tma_bench_reference_sums():
     assert tma_bench.expected_sums(64, 256, H.HGEMM_TMA_BULK, 32, 64, [1]) == (int(f.sum()), int((f * f).sum()))
 
 
+def test_stream_k_option_values():
+    # ragged 1000 x 3000 x 4104 on 2-SM 256 x 256 tiles: 48 tiles for 76 pairs.
+    # The estimate keeps whole tiles; stream_k = 2 splits them anyway; 0 never.
+    st, p = plan(1000, 3000, 4104, variant=3, stream_k=1)
+    assert st == ST_OK and p.stream_k == 0 and p.dp_tiles == 48
+    st, p = plan(1000, 3000, 4104, variant=3, stream_k=2)
+    assert st == ST_OK and p.stream_k == 1 and p.dp_tiles == 0 and p.sk_units == 48 * 65
+    st, p = plan(4096, 4096, 4096, variant=3, stream_k=2)
+    assert st == ST_OK and p.stream_k == 1 and p.dp_tiles == 152  # same split as the estimate picks
+    st, p = plan(4096, 4096, 4096, variant=3, stream_k=3)
+    assert st == ST_INV
+
+
 def test_work_list_arguments():
     st, p = plan(4096, 4096, 4096)
     assert H.hgemm_plan_work_item(p, -1, 0)[0] == ST_INV
