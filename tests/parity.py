@@ -66,6 +66,55 @@ def sample_entries(M: int, N: int, n_random: int, seed: int):
     return np.concatenate(rows), np.concatenate(cols)
 
 
+def sample_entries_sparse(M: int, N: int, n_random: int, seed: int, per_line: int = 2048):
+    """For outputs too large to check whole rows: n_random seeded entries plus
+    per_line seeded entries of every boundary row and column (including the
+    last row and column)."""
+    r = np.random.default_rng(seed)
+    rows = [r.integers(0, M, n_random)]
+    cols = [r.integers(0, N, n_random)]
+    for i in boundary_indices(M):
+        rows.append(np.full(per_line, i, np.int64))
+        cols.append(np.concatenate([[0, N - 1], r.integers(0, N, per_line - 2)]))
+    for j in boundary_indices(N):
+        rows.append(np.concatenate([[0, M - 1], r.integers(0, M, per_line - 2)]))
+        cols.append(np.full(per_line, j, np.int64))
+    return np.concatenate(rows), np.concatenate(cols)
+
+
+def check_gathered(C, A, B, M, N, K, layout, in_dtype, acc, out, n_random=8192, seed=0):
+    """Sampled parity for operands and results that stay on the device.
+
+    C, A, B are device tensors (A [M, K]; B [N, K] for TN, [K, N] for NN).
+    The sampled entries of C, and the rows of A and B they need, are gathered
+    to the host; the oracle computes those dot products from the exact input
+    bits (on the gathered sub-matrices, with the indices mapped)."""
+    import torch
+
+    rows, cols = sample_entries_sparse(M, N, n_random, seed)
+    ur, ri = np.unique(rows, return_inverse=True)
+    uc, ci = np.unique(cols, return_inverse=True)
+    dev = C.device
+    tr = torch.from_numpy(ur).to(dev)
+    tc = torch.from_numpy(uc).to(dev)
+    a_sub = A.view(torch.int16).index_select(0, tr).cpu().numpy().view(np.uint16)
+    if layout == "TN":
+        b_sub = B.view(torch.int16).index_select(0, tc).cpu().numpy().view(np.uint16)
+    else:
+        b_sub = B.view(torch.int16).index_select(1, tc).cpu().numpy().view(np.uint16)
+    g_bits = C.view(torch.int16)[torch.from_numpy(rows).to(dev), torch.from_numpy(cols).to(dev)]
+    g = oracle.decode(g_bits.cpu().numpy().view(np.uint16), out)
+    ref, absdot = oracle.gemm_entries(a_sub, b_sub, ur.size, uc.size, K, layout, in_dtype, ri, ci)
+    b = bound(ref, absdot, acc, out)
+    err = np.abs(g - ref)
+    bad = ~(err <= b)
+    if bad.any():
+        k = np.nonzero(bad)[0][:8]
+        detail = ", ".join("[%d,%d] gpu=%r ref=%r bound=%.3g" % (rows[i], cols[i], g[i], ref[i], b[i]) for i in k)
+        raise AssertionError("%d of %d sampled entries out of tolerance: %s" % (int(bad.sum()), ref.size, detail))
+    return dict(entries=int(ref.size), max_err=float(err.max()))
+
+
 def check(got_bits: np.ndarray, A_bits, B_bits, M, N, K, layout, in_dtype, acc, out, sampled=False, n_random=8192,
           seed=0, nthreads=0):
     """Compares a device result with the oracle.  Returns a dict of statistics
