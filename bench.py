@@ -225,9 +225,18 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--sweep", default=None, metavar="JSONL",
+                    help="measure every workload of the table (and --sweep-variants, --sweep-schedules), one JSON "
+                         "record per line appended to JSONL; records already there are skipped, so an "
+                         "interrupted sweep resumes")
+    ap.add_argument("--sweep-variants", default="auto")
+    ap.add_argument("--sweep-schedules", default="static")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.sweep:
+        sweep(args)
+        return
 
     world, rank, local = dist_setup()
     from tensor_core_half_gb300 import workloads
@@ -407,6 +416,111 @@ def main():
     }
     handle.close()
     print(json.dumps(out), flush=True)
+
+
+def sweep(args):
+    """Device-timed rate of every workload (one GPU), appended as JSON lines."""
+    import torch
+
+    from tensor_core_half_gb300 import hgemm, workloads
+
+    done = set()
+    if os.path.exists(args.sweep):
+        with open(args.sweep) as f:
+            for line in f:
+                if line.strip():
+                    r = json.loads(line)
+                    done.add((r["workload"], r["variant"], r["schedule"]))
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    props = torch.cuda.get_device_properties(dev)
+    peaks, peak_src = load_peaks()
+    names = sorted(workloads.WORKLOADS, key=lambda n: workloads.WORKLOADS[n].flops)
+    steps = args.steps if args.steps != 3000 else 200  # shorter default than the headline loop
+    n_new = 0
+    for name in names:
+        w = workloads.WORKLOADS[name]
+        metric, unit, per_step, bound = workload_metric(w)
+        a_cpu, b_cpu = None, None
+        for variant in args.sweep_variants.split(","):
+            for schedule in args.sweep_schedules.split(","):
+                if (name, variant, schedule) in done:
+                    continue
+                if a_cpu is None:
+                    a_cpu, b_cpu = workloads.generate_workload(w)
+                in_bytes = (a_cpu.numel() + b_cpu.numel()) * 2
+                c_bytes = w.M * w.N * 2
+                copies = max(1, math.ceil(2 * L2_BYTES / max(1, in_bytes + c_bytes)))
+                A = [a_cpu.to(dev) for _ in range(copies)]
+                B = [b_cpu.to(dev) for _ in range(copies)]
+                C = [torch.empty((w.M, w.N), dtype=workloads.DTYPES[w.out_dtype], device=dev) for _ in range(copies)]
+                h = hgemm.Handle()
+                h.set_option(hgemm.HGEMM_OPT_FORCE_VARIANT, hgemm.VARIANTS[variant])
+                h.set_option(hgemm.HGEMM_OPT_SCHEDULE, hgemm.SCHEDULES[schedule])
+                lay, fin, facc, fout = (hgemm.LAYOUTS[w.layout], hgemm.DTYPES[w.in_dtype], hgemm.DTYPES[w.acc_dtype],
+                                        hgemm.DTYPES[w.out_dtype])
+                st, plan = hgemm.hgemm_plan(w.M, w.N, w.K, lay, fin, facc, fout, props.multi_processor_count,
+                                            hgemm.VARIANTS[variant], 0, 1, schedule=hgemm.SCHEDULES[schedule])
+                if st != hgemm.HGEMM_OK:  # e.g. a forced variant that does not take this layout
+                    rec = {"workload": name, "variant": variant, "schedule": schedule,
+                           "status": hgemm.hgemm_status_string(st)}
+                else:
+                    sp = torch.cuda.current_stream(dev).cuda_stream
+
+                    def step(i):
+                        s = hgemm.hgemm_run(h.h, A[i % copies].data_ptr(), B[i % copies].data_ptr(),
+                                            C[i % copies].data_ptr(), w.M, w.N, w.K, lay, fin, facc, fout, sp)
+                        if s != hgemm.HGEMM_OK:
+                            raise hgemm.HgemmError(s, "hgemm_run")
+
+                    for i in range(args.warmup):
+                        step(i)
+                    torch.cuda.synchronize(dev)
+                    sampler = ClockSampler(0)
+                    time.sleep(0.2)
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    h0 = time.time()
+                    e0.record()
+                    for i in range(steps):
+                        step(i)
+                    e1.record()
+                    torch.cuda.synchronize(dev)
+                    h1 = time.time()
+                    sampler.stop()
+                    ms = e0.elapsed_time(e1) / steps
+                    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                          for _ in range(50)]
+                    for i, (x, y) in enumerate(ev):
+                        x.record()
+                        step(i)
+                        y.record()
+                    torch.cuda.synchronize(dev)
+                    single = sorted(x.elapsed_time(y) for x, y in ev)
+                    st, detail = h.sync_status()
+                    if st != hgemm.HGEMM_OK:
+                        raise hgemm.HgemmError(st, "sweep %s (detail %s)" % (name, hex(detail)))
+                    value = per_step / (ms / 1e3)
+                    peak = peaks.get("bf16_tflops") if bound == "tensor" else peaks.get("hbm_gbs")
+                    rec = {"workload": name, "variant": variant, "schedule": schedule, "metric": metric,
+                           "value": round(value, 3), "unit": unit, "steps": steps, "ms_per_step": round(ms, 5),
+                           "single_launch_ms": {"p10": round(single[5], 5), "median": round(single[25], 5),
+                                                "p90": round(single[45], 5)},
+                           "roofline": {"bound": bound, "peak": peak, "frac": round(value / peak, 4),
+                                        "peak_source": "%s%s" % (peak_src, " burst" if bound == "tensor" else "")},
+                           "plan": {"variant": list(hgemm.VARIANTS)[plan.variant], "grid": plan.grid,
+                                    "tile": [plan.tile_m, plan.tile_n], "stages": plan.stages,
+                                    "stream_k": bool(plan.stream_k), "work_ids": plan.work_ids,
+                                    "splitk_chunks": plan.splitk_chunks},
+                           "gpu": props.name, "sms": props.multi_processor_count,
+                           "clocks": sampler.summary(h0, h1)}
+                h.close()
+                del A, B, C
+                torch.cuda.empty_cache()
+                with open(args.sweep, "a") as f:
+                    f.write(json.dumps(rec) + "\n")
+                n_new += 1
+    print(json.dumps({"sweep": args.sweep, "records_added": n_new, "records_skipped": len(done)}), flush=True)
 
 
 def run_reference(args, w, metric, unit, per_step, world, rank):
