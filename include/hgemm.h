@@ -46,7 +46,9 @@ typedef enum {
   HGEMM_ERR_NO_DEVICE = 5,   /* no CUDA device / driver */
   HGEMM_ERR_CUDA = 6,        /* a CUDA runtime or driver call failed */
   HGEMM_ERR_TIMEOUT = 7,     /* a bounded device-side wait gave up (reported by hgemm_sync_status) */
-  HGEMM_ERR_OOM = 8          /* workspace allocation failed */
+  HGEMM_ERR_OOM = 8,         /* workspace allocation failed */
+  HGEMM_ERR_CHECK = 9        /* a device-side invariant check failed (HGEMM_OPT_CHECKS; reported by
+                                hgemm_sync_status, which gives the check's number in detail bits 8-15) */
 } hgemm_status_t;
 
 typedef enum { HGEMM_LAYOUT_TN = 0, HGEMM_LAYOUT_NN = 1 } hgemm_layout_t;
@@ -68,7 +70,10 @@ typedef enum {
   HGEMM_OPT_FORCE_VARIANT = 1, /* value: an hgemm_variant_t; AUTO restores automatic choice   */
   HGEMM_OPT_TIMEOUT_NS = 2,    /* value: limit of every device-side wait, ns (default 2e9)    */
   HGEMM_OPT_INJECT_FAULT = 3,  /* value: 0 off; 1 = the first CTA's producer drops its first
-                                  stage, so the consumer's bounded wait must give up (tests)  */
+                                  stage, so the consumer's bounded wait must give up; 2 = the
+                                  host fills the fix-up ticket counters with 0x01 bytes before
+                                  a stream-K or split-K launch, which HGEMM_OPT_CHECKS must
+                                  report (tests)                                              */
   HGEMM_OPT_GROUP_M = 4,       /* value: rasterisation group height in tiles (default 8)      */
   HGEMM_OPT_MAX_CTAS = 5,      /* value: cap on persistent CTAs (0 = one per SM)              */
   HGEMM_OPT_STREAM_K = 6,      /* value: 1 (default) lets the planner split the last wave of
@@ -78,8 +83,22 @@ typedef enum {
   HGEMM_OPT_TRACE = 7,         /* value: capacity in events of a device trace buffer that the
                                   kernels append to (0 = off, the default); hgemm_trace_read */
   HGEMM_OPT_SCHEDULE = 8,      /* value: an hgemm_schedule_t for the dense kernels           */
-  HGEMM_OPT_EPILOGUE = 9       /* value: an hgemm_epilogue_t for the dense kernels           */
+  HGEMM_OPT_EPILOGUE = 9,      /* value: an hgemm_epilogue_t for the dense kernels           */
+  HGEMM_OPT_CHECKS = 10        /* value: 1 = the kernels check their invariants (work ids from
+                                  launch control in range, work items and tiles in range,
+                                  fix-up tickets not past the contributor count, partial
+                                  slots in range) and report a violation as HGEMM_ERR_CHECK
+                                  instead of trapping; 0 (default) = no checks              */
 } hgemm_option_t;
+
+/* Check numbers reported with HGEMM_ERR_CHECK (detail bits 8-15). */
+typedef enum {
+  HGEMM_CHECK_WORK_ID = 1,     /* a work id or chunk from launch control out of range */
+  HGEMM_CHECK_ITEM = 2,        /* a work item's tile or k-block range out of range    */
+  HGEMM_CHECK_TICKET = 3,      /* a fix-up ticket past the tile's contributor count   */
+  HGEMM_CHECK_CONTRIBUTOR = 4, /* the item's owner outside the tile's contributors    */
+  HGEMM_CHECK_PARTIAL = 5      /* a partial-sum slot outside the workspace            */
+} hgemm_check_t;
 
 /*
  * How the dense kernels' epilogue writes C (HGEMM_OPT_EPILOGUE); both give

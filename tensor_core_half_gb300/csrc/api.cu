@@ -49,6 +49,7 @@ struct Ctx {
   int stream_k = 1;  // 0 never, 1 when the estimate says so, 2 whenever the tile count leaves a partial wave
   int schedule = HGEMM_SCHEDULE_STATIC;
   int epilogue = HGEMM_EPILOGUE_TMA_STORE;
+  bool checks = false;
   TraceBuf* trace = nullptr;  // device trace buffer (HGEMM_OPT_TRACE)
   int64_t trace_capacity = 0;
   // hgemm_run_host: two staging sets (double buffering across calls), three
@@ -302,6 +303,17 @@ hgemm_status_t ensure_workspace(Ctx* c, size_t partial_bytes, size_t n_tiles, cu
   return HGEMM_OK;
 }
 
+// HGEMM_OPT_INJECT_FAULT = 2 (tests): fill the fix-up ticket counters with
+// 0x01 bytes, so every ticket is far past its tile's contributor count.  The
+// kernels only compare tickets, so nothing is accessed out of range and no
+// wait depends on them; HGEMM_OPT_CHECKS reports HGEMM_ERR_CHECK.  The next
+// launch zeroes the counters again.
+hgemm_status_t inject_ticket_fault(Ctx* c, cudaStream_t s) {
+  if (c->inject != 2) return HGEMM_OK;
+  c->tickets_dirty = true;
+  return cuda_status(cudaMemsetAsync(c->tickets, 0x01, c->ticket_count * sizeof(int32_t), s));
+}
+
 }  // namespace
 
 struct hgemm_ctx : Ctx {};
@@ -319,6 +331,7 @@ const char* hgemm_status_string(hgemm_status_t s) {
     case HGEMM_ERR_CUDA: return "HGEMM_ERR_CUDA: a CUDA call failed";
     case HGEMM_ERR_TIMEOUT: return "HGEMM_ERR_TIMEOUT: a device-side wait gave up";
     case HGEMM_ERR_OOM: return "HGEMM_ERR_OOM: device allocation failed";
+    case HGEMM_ERR_CHECK: return "HGEMM_ERR_CHECK: a device-side invariant check failed";
   }
   return "unknown hgemm status";
 }
@@ -489,7 +502,7 @@ hgemm_status_t hgemm_set_option(hgemm_handle_t h, int32_t option, int64_t value)
       h->timeout_ns = (uint64_t)value;
       return HGEMM_OK;
     case HGEMM_OPT_INJECT_FAULT:
-      if (value < 0 || value > 1) return HGEMM_ERR_INVALID_ARG;
+      if (value < 0 || value > 2) return HGEMM_ERR_INVALID_ARG;
       h->inject = (int)value;
       return HGEMM_OK;
     case HGEMM_OPT_GROUP_M:
@@ -507,6 +520,10 @@ hgemm_status_t hgemm_set_option(hgemm_handle_t h, int32_t option, int64_t value)
     case HGEMM_OPT_SCHEDULE:
       if (value != HGEMM_SCHEDULE_STATIC && value != HGEMM_SCHEDULE_DYNAMIC) return HGEMM_ERR_INVALID_ARG;
       h->schedule = (int)value;
+      return HGEMM_OK;
+    case HGEMM_OPT_CHECKS:
+      if (value < 0 || value > 1) return HGEMM_ERR_INVALID_ARG;
+      h->checks = value != 0;
       return HGEMM_OK;
     case HGEMM_OPT_EPILOGUE:
       if (value != HGEMM_EPILOGUE_TMA_STORE && value != HGEMM_EPILOGUE_DIRECT) return HGEMM_ERR_INVALID_ARG;
@@ -566,6 +583,7 @@ hgemm_status_t hgemm_run(hgemm_handle_t h, const void* A, const void* B, void* C
     const size_t partial_bytes = (size_t)p.splitk_chunks * 2 * 128 * (size_t)mma_n * sizeof(float);
     st = ensure_workspace(h, partial_bytes, (size_t)p.num_tiles * 2, s);  // one arrival counter per tile, spare
     if (st != HGEMM_OK) return st;
+    if ((st = inject_ticket_fault(h, s)) != HGEMM_OK) return st;
     if (p.smem_bytes > h->splitk_prepared_smem) return HGEMM_ERR_UNSUPPORTED;
     SplitKArgs args;
     args.M = (int32_t)M;
@@ -579,6 +597,7 @@ hgemm_status_t hgemm_run(hgemm_handle_t h, const void* A, const void* B, void* C
     args.big = p.grid;
     args.n_small = p.splitk_chunks - p.grid;
     args.dynamic = h->schedule == HGEMM_SCHEDULE_DYNAMIC ? 1 : 0;
+    args.checks = h->checks ? 1 : 0;
     args.stages = p.stages;
     args.idesc = make_idesc(128, mma_n, in_dtype == HGEMM_BF16, true, false, false);
     args.out_bf16 = out_dtype == HGEMM_BF16;
@@ -626,6 +645,7 @@ hgemm_status_t hgemm_run(hgemm_handle_t h, const void* A, const void* B, void* C
   args.sk_units = p.sk_units;
   args.dynamic = h->schedule == HGEMM_SCHEDULE_DYNAMIC ? 1 : 0;
   args.epi_direct = h->epilogue == HGEMM_EPILOGUE_DIRECT ? 1 : 0;
+  args.checks = h->checks ? 1 : 0;
   args.C = C;
   args.partials = nullptr;
   args.tickets = nullptr;
@@ -635,6 +655,7 @@ hgemm_status_t hgemm_run(hgemm_handle_t h, const void* A, const void* B, void* C
     // two counters per tile and CTA of the pair: arrivals, then publications
     st = ensure_workspace(h, partial_bytes, (size_t)p.num_tiles * (size_t)info.cta_group * 2, s);
     if (st != HGEMM_OK) return st;
+    if ((st = inject_ticket_fault(h, s)) != HGEMM_OK) return st;
     args.partials = h->partials;
     args.tickets = h->tickets;
   }

@@ -86,6 +86,8 @@ struct IdFeed {
   ClcIds<CG, SLOTS> clc;
   int32_t cluster, nclusters;
   bool dynamic;
+  bool checks;
+  int32_t* status;
   bool started = false, finished = false;
   bool want = false;  // issuer: the current id's request is still to be made
 
@@ -95,7 +97,9 @@ struct IdFeed {
         clc(resp0, full0, empty0, issuer, warp_wide, arrive),
         cluster(cluster_),
         nclusters(nclusters_),
-        dynamic(a.dynamic != 0) {}
+        dynamic(a.dynamic != 0),
+        checks(a.checks != 0),
+        status(a.status) {}
 
   // 1: an item in w; 0: no work left; -1: a wait gave up.
   __device__ int next(WorkItem& w, const WaitCtl& ctl) {
@@ -119,6 +123,10 @@ struct IdFeed {
       int64_t id = 0;
       const int got = clc.fetch(&id, ctl);
       if (got < 0) return -1;
+      if (got > 0 && checks && (id < 0 || id >= it.n_ids)) {
+        report_check(status, kCheckWorkId, nullptr);
+        return -1;
+      }
       if (got == 0) {
         finished = true;
         started = false;
@@ -233,6 +241,17 @@ __global__ void __launch_bounds__(192, 1)
         trace_event(tb, kRoleProducer, kTraceItemBegin, w.tile, w.kb0);
         uint32_t stall = 0;
         const TileCoord tc = tile_coord(w.tile, args.tiles_m, args.tiles_n, args.group_m);
+        if (args.checks) {
+          const bool bad = w.tile < 0 || w.tile >= args.num_tiles || w.kb0 < 0 || w.kb0 >= w.kb1 ||
+                           w.kb1 > args.k_blocks || tc.m < 0 || tc.m >= args.tiles_m || tc.n < 0 ||
+                           tc.n >= args.tiles_n ||
+                           (w.slot >= 0 && (w.tile < args.dp_tiles || w.owner < 0 || w.owner >= args.sk_ranges));
+          if (bad) {
+            report_check(args.status, kCheckItem, abort_flag);
+            ok = false;
+            break;
+          }
+        }
         const int m_row = tc.m * (S::BM * CG) + (int)rank * S::BM;
         const int n_row = tc.n * BN + (int)rank * S::B_ROWS;
         for (int kb = w.kb0; kb < w.kb1; ++kb) {
@@ -507,6 +526,14 @@ __global__ void __launch_bounds__(192, 1)
         named_bar_sync(1, 128);
         const int32_t ticket = *ticket_slot;
         named_bar_sync(1, 128);
+        if (args.checks && threadIdx.x == 64) {
+          // A ticket past the count would leave the tile unreduced; the owner
+          // and its partial slots must lie inside the contributor range and
+          // the workspace.
+          if (ticket < 0 || ticket > others) report_check(args.status, kCheckTicket, abort_flag);
+          if (w.owner < c_first || w.owner > c_last) report_check(args.status, kCheckContributor, abort_flag);
+          if (c_first < 0 || c_last >= args.sk_ranges) report_check(args.status, kCheckPartial, abort_flag);
+        }
         if (ticket != others) {
           float4* mine = partial_of(w.owner, w.slot) + row;
 #pragma unroll 1

@@ -108,13 +108,19 @@ struct ChunkFeed {
   SplitChunks ch;
   int32_t k_blocks;
   bool dynamic;
+  bool checks;
+  int32_t* status;
   bool started = false, finished = false;
   bool want = false;  // issuer: the current chunk's request is still to be made
   int64_t chunk = -1, begin = 0, u = 0, end = 0;
 
   __device__ ChunkFeed(const SplitKArgs& a, uint32_t resp0, uint32_t full0, uint32_t empty0, bool issuer,
                        bool warp_wide, bool arrive)
-      : clc(resp0, full0, empty0, issuer, warp_wide, arrive), k_blocks(a.k_blocks), dynamic(a.dynamic != 0) {
+      : clc(resp0, full0, empty0, issuer, warp_wide, arrive),
+        k_blocks(a.k_blocks),
+        dynamic(a.dynamic != 0),
+        checks(a.checks != 0),
+        status(a.status) {
     ch.units = a.units;
     ch.head = a.head;
     ch.big = a.big;
@@ -154,6 +160,10 @@ struct ChunkFeed {
       int64_t g = 0;
       const int got = clc.fetch(&g, ctl);
       if (got < 0) return -1;
+      if (got > 0 && checks && (g < 0 || g >= ch.count())) {
+        report_check(status, kCheckWorkId, nullptr);
+        return -1;
+      }
       if (got == 0) {
         finished = true;
         return 0;
@@ -304,6 +314,12 @@ __global__ void __launch_bounds__(192, 1)
         if (more < 0) ok = false;
         if (more <= 0) break;
         trace_event(tb, kRoleProducer, kTraceItemBegin, sg.tile, sg.kb0);
+        if (args.checks && (sg.tile < 0 || sg.tile >= args.n_tiles || sg.kb0 < 0 || sg.kb0 >= sg.kb1 ||
+                            sg.kb1 > args.k_blocks || sg.chunk < 0 || sg.chunk >= chunks.count())) {
+          report_check(args.status, kCheckItem, abort_flag);
+          ok = false;
+          break;
+        }
         for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, ctl)) {
             ok = false;
@@ -476,6 +492,11 @@ __global__ void __launch_bounds__(192, 1)
         if (threadIdx.x == 64) *ticket_slot = atom_add_acq_rel_gpu(arrivals, 1);  // ... before the ticket
         named_bar_sync(1, 128);  // ... and the acquire orders the partial reads below
         const int32_t ticket = *ticket_slot;
+        if (args.checks && threadIdx.x == 64) {
+          if (ticket < 0 || ticket > others) report_check(args.status, kCheckTicket, abort_flag);
+          if (sg.chunk < c_first || sg.chunk > c_last) report_check(args.status, kCheckContributor, abort_flag);
+          if (c_first < 0 || c_last >= chunks.count()) report_check(args.status, kCheckPartial, abort_flag);
+        }
         if (ticket == others) {
           float s[kSplitKMaxM];
 #pragma unroll

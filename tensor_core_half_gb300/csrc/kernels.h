@@ -9,6 +9,9 @@ namespace hg {
 
 // Device status word layout (shared with hgemm_sync_status).
 constexpr int32_t kStatusTimeout = 7;  // == HGEMM_ERR_TIMEOUT
+constexpr int32_t kStatusCheck = 9;    // == HGEMM_ERR_CHECK
+// Invariant checks (== hgemm_check_t)
+enum CheckId : int32_t { kCheckWorkId = 1, kCheckItem = 2, kCheckTicket = 3, kCheckContributor = 4, kCheckPartial = 5 };
 enum Role : int32_t { kRoleProducer = 1, kRoleMma = 2, kRoleEpilogue = 3, kRoleTeardown = 4 };
 
 // Intra-kernel event trace (HGEMM_OPT_TRACE): a device buffer of fixed-size
@@ -50,6 +53,7 @@ struct DenseArgs {
   int64_t sk_units;   // (num_tiles - dp_tiles) * k_blocks, split evenly over the ranges
   int32_t dynamic;    // 1: one cluster per work id, ids taken over by cluster launch control
   int32_t epi_direct; // 1: the epilogue stores C from registers (16-byte stores), no TMA store
+  int32_t checks;     // 1: check invariants, report violations as kStatusCheck
   void* C;            // [M][N] row-major output (used by the direct epilogue)
   float* partials;    // stream-K partials [sk_ranges][2][cta_group][BN/4][128] float4 (null if sk_units == 0)
   int32_t* tickets;  // [2][num_tiles * cta_group] arrivals, publications; all zero between launches
@@ -91,6 +95,7 @@ struct SplitKArgs {
   int32_t big;       // big chunks (= CTAs of the static schedule)
   int32_t n_small;   // small chunks after them (dynamic schedule), else 0
   int32_t dynamic;   // 1: one CTA per chunk, chunks taken over by cluster launch control
+  int32_t checks;    // 1: check invariants, report violations as kStatusCheck
   int32_t stages;
   uint32_t idesc;
   int32_t out_bf16;

@@ -176,6 +176,7 @@ extern "C" hgemm_status_t hgemm_run_splitk_noalloc(const void* A, const void* B,
   args.big = (int32_t)grid;
   args.n_small = 0;
   args.dynamic = 0;
+  args.checks = 0;
   args.stages = stages;
   args.idesc = hg::make_idesc(128, mma_n, in_dtype == HGEMM_BF16, true, false, false);
   args.out_bf16 = out_dtype == HGEMM_BF16;

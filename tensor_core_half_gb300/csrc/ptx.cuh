@@ -190,6 +190,13 @@ __device__ __forceinline__ bool mbar_wait_stall(uint32_t bar, uint32_t parity, c
   return ok;
 }
 
+// A failed invariant check (HGEMM_OPT_CHECKS): the first failure is kept in
+// the status word; the CTA's other roles stop waiting through the abort flag.
+__device__ __forceinline__ void report_check(int32_t* status, int32_t check, volatile uint32_t* abort_flag) {
+  if (abort_flag) *abort_flag = 1u;
+  atomicCAS(status, 0, 9 /* HGEMM_ERR_CHECK */ | (check << 8) | ((int32_t)(blockIdx.x & 0xFFFF) << 16));
+}
+
 // ------------------------------------------------- cluster launch control ----
 // A request to cancel the launch of a cluster of this grid that has not
 // started yet.  The 16-byte response lands at `resp` (shared memory of this

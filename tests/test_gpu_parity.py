@@ -366,6 +366,56 @@ def test_bounded_wait_gives_up_and_recovers(h, variant, M, schedule):
     parity.check(got, ab, bb, M, N, K, "TN", "bf16", "f32", "bf16")
 
 
+# Checked mode (HGEMM_OPT_CHECKS): valid runs of every kind report nothing.
+CHECKED_CASES = [("2sm256", "TN", 4096, 4096, 256, 2, "static"), ("2sm256", "TN", 4096, 4096, 256, 2, "dynamic"),
+                 ("1sm128", "NN", 1000, 3000, 520, 1, "dynamic"), ("2sm192", "TN", 1000, 3000, 4104, 1, "static"),
+                 ("1sm256", "TN", 2048, 4096, 192, 1, "dynamic"), ("2sm256", "NN", 768, 520, 4104, 1, "static"),
+                 ("splitk", "TN", 16, 16384, 4096, 1, "static"), ("splitk", "TN", 40, 8192, 8192, 1, "dynamic")]
+
+
+@pytest.mark.parametrize("variant,layout,M,N,K,sk,schedule", CHECKED_CASES)
+def test_checked_runs_report_nothing(h, variant, layout, M, N, K, sk, schedule):
+    a, b, ab, bb = parity.inputs(M, N, K, layout, "bf16", ("normal", 1.0), 88)
+    h.set_option(hgemm.HGEMM_OPT_CHECKS, 1)
+    try:
+        got = run(h, a, b, M, N, K, layout, "f32", "bf16", variant, stream_k=sk, schedule=schedule)
+    finally:
+        h.set_option(hgemm.HGEMM_OPT_CHECKS, 0)
+    parity.check(got, ab, bb, M, N, K, layout, "bf16", "f32", "bf16")
+
+
+@pytest.mark.parametrize("variant,M,N,K,schedule", [("2sm256", 4096, 4096, 256, "static"),
+                                                    ("2sm256", 4096, 4096, 256, "dynamic"),
+                                                    ("splitk", 16, 16384, 4096, "static"),
+                                                    ("splitk", 16, 16384, 4096, "dynamic")])
+def test_checks_catch_corrupted_tickets(h, variant, M, N, K, schedule):
+    # The host fills the fix-up ticket counters with 0x01 bytes before the
+    # launch: every ticket is then far past its tile's contributor count.  The
+    # kernels only compare tickets (no access depends on them, no wait), so the
+    # launch ends; the checks must report it.  The next launch is correct.
+    a, b, ab, bb = parity.inputs(M, N, K, "TN", "bf16", ("normal", 1.0), 89)
+    A, B = a.cuda(), b.cuda()
+    C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    h.set_option(hgemm.HGEMM_OPT_FORCE_VARIANT, hgemm.VARIANTS[variant])
+    h.set_option(hgemm.HGEMM_OPT_SCHEDULE, hgemm.SCHEDULES[schedule])
+    h.set_option(hgemm.HGEMM_OPT_STREAM_K, 2)  # split the dense tiles even where the estimate would not
+    h.set_option(hgemm.HGEMM_OPT_CHECKS, 1)
+    h.set_option(hgemm.HGEMM_OPT_INJECT_FAULT, 2)
+    try:
+        h.run(A, B, C, layout="TN", acc="f32")
+        st, detail = h.sync_status()
+        assert st == hgemm.HGEMM_ERR_CHECK, (st, hex(detail))
+        assert (detail & 0xFF) == hgemm.HGEMM_ERR_CHECK and ((detail >> 8) & 0xFF) == hgemm.HGEMM_CHECK_TICKET
+    finally:
+        h.set_option(hgemm.HGEMM_OPT_INJECT_FAULT, 0)
+        h.set_option(hgemm.HGEMM_OPT_CHECKS, 0)
+        h.set_option(hgemm.HGEMM_OPT_STREAM_K, 1)
+        h.set_option(hgemm.HGEMM_OPT_SCHEDULE, hgemm.HGEMM_SCHEDULE_STATIC)
+        h.set_option(hgemm.HGEMM_OPT_FORCE_VARIANT, hgemm.HGEMM_VARIANT_AUTO)
+    got = run(h, a, b, M, N, K, "TN", "f32", "bf16", variant, stream_k=2, schedule=schedule)
+    parity.check(got, ab, bb, M, N, K, "TN", "bf16", "f32", "bf16")
+
+
 @pytest.mark.parametrize("pinned", [True, False], ids=["pinned", "pageable"])
 @pytest.mark.parametrize("layout", ["TN", "NN"])
 @pytest.mark.parametrize("M,N,K", [(1000, 1000, 1024), (3000, 520, 200), (16, 2048, 4096), (5, 8, 0)])

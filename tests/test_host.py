@@ -21,7 +21,7 @@ def test_library_exports_every_declared_symbol():
 
 
 def test_status_strings():
-    for s in range(0, 9):
+    for s in range(0, 10):
         assert H.hgemm_status_string(s).startswith("HGEMM_")
     assert "unknown" in H.hgemm_status_string(99)
     assert H.hgemm_version() >= 100
