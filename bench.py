@@ -71,8 +71,9 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def load_traffic(workload: str, variant: int):
-    """DRAM bytes per launch from a committed ncu summary, if it matches these kernels."""
+def load_traffic(workload: str, variant: int, plan=None):
+    """DRAM bytes per launch from a committed ncu summary, if it matches these
+    kernels and this launch plan (the stream-K split changes the traffic)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -82,6 +83,11 @@ def load_traffic(workload: str, variant: int):
     kernel = "splitk" if variant == 4 else "dense"
     if not e or e.get("kernel_hash") != kernel_source_hash(kernel):
         return None
+    want = e.get("plan")
+    if plan is not None and want is not None:
+        have = {"grid": plan.grid, "dp_tiles": plan.dp_tiles, "sk_units": plan.sk_units}
+        if any(have[k] != v for k, v in want.items()):
+            return None
     return e.get("dram_bytes_per_launch")
 
 
@@ -383,7 +389,7 @@ def main():
         achieved = (w.compulsory_bytes / 1e9) / (kernel_ms_avg / 1e3)
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "peak_source": peak_src}
-    roof["traffic"] = load_traffic(w.name, plan.variant)
+    roof["traffic"] = load_traffic(w.name, plan.variant, plan)
     roof["kernel_ms_avg"] = round(kernel_ms_avg, 5)
 
     cpu = None

@@ -72,7 +72,7 @@ def test_plan_variant_choice():
     assert (p.tile_m, p.tile_n, p.tiles_m, p.tiles_n, p.num_tiles, p.k_blocks) == (256, 256, 16, 16, 256, 64)
     assert p.grid == 152 and p.tmem_cols == 512 and p.smem_bytes <= 232448
     # 256 tiles over 76 pairs: two whole waves data-parallel, the rest stream-K
-    assert p.stream_k == 1 and p.dp_tiles == 152 and p.sk_units == (256 - 152) * 64
+    assert p.stream_k == 1 and p.dp_tiles == 228 and p.sk_units == (256 - 228) * 64  # remainder of 28 tiles split
     st, p = plan(4096, 4096, 4096, stream_k=0, variant=3)
     assert st == ST_OK and p.stream_k == 0 and p.dp_tiles == 256 and p.sk_units == 0 and p.workspace_bytes == 0
     # a tile count that is a whole number of waves stays data-parallel
@@ -335,6 +335,16 @@ def test_tma_bench_reference_sums():
     assert tma_bench.expected_sums(64, 256, H.HGEMM_TMA_BULK, 32, 64, [1]) == (int(f.sum()), int((f * f).sum()))
 
 
+def test_stream_k_split_by_remainder():
+    # 2-SM 256 x 256 tiles, 76 pairs.  86 tiles: a remainder of 10 (< 76 / 4)
+    # would be cut among ~8 pairs each, so the whole first round joins the split.
+    st, p = plan(512, 256 * 43, 4096, variant=3)
+    assert st == ST_OK and p.num_tiles == 86 and p.stream_k == 1 and p.dp_tiles == 0 and p.sk_units == 86 * 64
+    # 106 tiles: a remainder of 30 (>= 19) is split alone; 76 tiles stay whole.
+    st, p = plan(512, 256 * 53, 4096, variant=3)
+    assert st == ST_OK and p.num_tiles == 106 and p.stream_k == 1 and p.dp_tiles == 76 and p.sk_units == 30 * 64
+
+
 def test_stream_k_option_values():
     # ragged 1000 x 3000 x 4104 on 2-SM 256 x 256 tiles: 48 tiles for 76 pairs.
     # The estimate keeps whole tiles; stream_k = 2 splits them anyway; 0 never.
@@ -343,7 +353,7 @@ def test_stream_k_option_values():
     st, p = plan(1000, 3000, 4104, variant=3, stream_k=2)
     assert st == ST_OK and p.stream_k == 1 and p.dp_tiles == 0 and p.sk_units == 48 * 65
     st, p = plan(4096, 4096, 4096, variant=3, stream_k=2)
-    assert st == ST_OK and p.stream_k == 1 and p.dp_tiles == 152  # same split as the estimate picks
+    assert st == ST_OK and p.stream_k == 1 and p.dp_tiles == 228  # same split as the estimate picks
     st, p = plan(4096, 4096, 4096, variant=3, stream_k=3)
     assert st == ST_INV
 
