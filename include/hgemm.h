@@ -179,10 +179,17 @@ hgemm_status_t hgemm_destroy(hgemm_handle_t h);
  * pitch is a multiple of 16 bytes, a TMA requirement).  K == 0 skips the K
  * check and A, B may then be null.
  * Asynchronous: returns once the kernel is enqueued.  A device-side timeout
- * is reported later by hgemm_sync_status.  Split-K launches use a workspace
- * that the handle allocates on first use (cudaMalloc; HGEMM_ERR_OOM on
- * failure); consecutive launches on different streams must not overlap when
- * they share a handle.
+ * is reported later by hgemm_sync_status.  Split-K and stream-K launches use a
+ * workspace that the handle allocates on first use (cudaMalloc; HGEMM_ERR_OOM
+ * on failure); consecutive launches on different streams must not overlap
+ * when they share a handle.
+ * CUDA graphs: hgemm_run may be captured into a graph.  A capture cannot
+ * contain the workspace allocation, so warm the handle up outside the
+ * capture with the largest problem the graph will hold; during a capture a
+ * call whose workspace would have to grow returns HGEMM_ERR_UNSUPPORTED and
+ * enqueues nothing.  Replays use the handle's workspace, so replays of graphs
+ * holding launches of one handle must not overlap each other or other
+ * launches of that handle.
  */
 hgemm_status_t hgemm_run(hgemm_handle_t h, const void* A, const void* B, void* C, int64_t M, int64_t N,
                          int64_t K, hgemm_layout_t layout, hgemm_dtype_t in_dtype, hgemm_dtype_t acc_dtype,

@@ -283,8 +283,17 @@ hgemm_status_t cuda_status(cudaError_t e) {
   return HGEMM_ERR_CUDA;
 }
 
+bool stream_capturing(cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  return cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs != cudaStreamCaptureStatusNone;
+}
+
 // Partial sums and tickets shared by split-K and stream-K launches of a handle.
+// While `s` is being captured into a CUDA graph nothing may be allocated or
+// freed: a workspace that would have to grow is refused (UNSUPPORTED).
 hgemm_status_t ensure_workspace(Ctx* c, size_t partial_bytes, size_t n_tiles, cudaStream_t s) {
+  if ((c->partials_bytes < partial_bytes || c->ticket_count < n_tiles) && stream_capturing(s))
+    return HGEMM_ERR_UNSUPPORTED;
   if (c->partials_bytes < partial_bytes) {
     if (c->partials) cudaFree(c->partials);
     c->partials = nullptr;
