@@ -607,7 +607,6 @@ __global__ void __launch_bounds__(192, 1)
   }
 
   // --------------------------------------------------------- teardown ----
-  if (threadIdx.x == 0) trace_event(tb, 0, kTraceKernelEnd, -1, (int32_t)(clock64() & 0x7fffffff));
   if constexpr (CG == 2) {
     // In a pair, the peer's loads signal CTA 0 and CTA 0's MMAs read the peer's
     // shared memory; after a give-up, leave time for copies still in flight.
@@ -620,6 +619,8 @@ __global__ void __launch_bounds__(192, 1)
   } else {
     __syncthreads();
   }
+  // every role of the CTA (pair) is done: the end of the CTA's work
+  if (threadIdx.x == 0) trace_event(tb, 0, kTraceKernelEnd, -1, (int32_t)(clock64() & 0x7fffffff));
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc<CG>(tmem_base, S::TMEM_COLS);

@@ -521,8 +521,9 @@ __global__ void __launch_bounds__(192, 1)
     if (!ok && lane == 0) sk_report(args.status, kRoleEpilogue, abort_flag);
   }
 
-  if (threadIdx.x == 0) trace_event(tb, 0, kTraceKernelEnd, -1, (int32_t)(clock64() & 0x7fffffff));
   __syncthreads();
+  // every role of the CTA is done: the end of the CTA's work
+  if (threadIdx.x == 0) trace_event(tb, 0, kTraceKernelEnd, -1, (int32_t)(clock64() & 0x7fffffff));
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc<1>(tmem_base, (uint32_t)tmem_cols);
