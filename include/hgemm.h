@@ -79,7 +79,10 @@ typedef enum {
   HGEMM_OPT_STREAM_K = 6,      /* value: 1 (default) lets the planner split the last wave of
                                   dense tiles along K (stream-K) when its estimate favours it;
                                   0 keeps every tile whole; 2 splits whenever the tile count
-                                  leaves a partial wave                                      */
+                                  leaves a partial wave.  Split-K (skinny M) plans likewise:
+                                  1 chooses between whole tiles per CTA and the balanced
+                                  K split over every SM by estimate, 0 always takes whole
+                                  tiles, 2 always splits                                     */
   HGEMM_OPT_TRACE = 7,         /* value: capacity in events of a device trace buffer that the
                                   kernels append to (0 = off, the default); hgemm_trace_read */
   HGEMM_OPT_SCHEDULE = 8,      /* value: an hgemm_schedule_t for the dense kernels           */
@@ -136,8 +139,8 @@ typedef enum { HGEMM_SCHEDULE_STATIC = 0, HGEMM_SCHEDULE_DYNAMIC = 1 } hgemm_sch
  * nanosecond timer.  role: 0 CTA, 1 TMA producer, 2 MMA issuer, 3 epilogue.
  * kind: 1 kernel begin, 2 kernel end (after setup / before teardown; value =
  * the SM cycle counter's low 31 bits, so cycles / ns gives the clock), 3 item
- * begin, 4 item end, 5 stream-K partial stored (value = ticket drawn), 6 split
- * tile reduced (value = contributors), 7 cycles the role spent blocked on its
+ * begin, 4 item end, 5 stream-K or split-K partial stored and its ticket
+ * drawn (value = ticket), 6 split tile reduced (value = contributors), 7 cycles the role spent blocked on its
  * barriers during the item (value).  item = tile index (-1 if none); value
  * for item begin/end = first / last k-block (epilogue: the stream-K slot). */
 typedef struct {
@@ -269,6 +272,8 @@ typedef struct {
   int64_t splitk_head_units; /* split-K: units in chunks [0, grid) (all of them under STATIC;
                                 under DYNAMIC about 3/4, the rest in splitk_chunks - grid
                                 small chunks)                                             */
+  int32_t splitk_align;  /* split-K: k_blocks when every chunk is whole tiles (no tile's K
+                            range is split, no partials or fix-up), else 1                */
 } hgemm_plan_t;
 
 /*
@@ -324,6 +329,19 @@ hgemm_status_t hgemm_plan_tile(const hgemm_plan_t* plan, int32_t t, int32_t* til
  * and the small chunks after them go to whichever CTA finishes first.
  */
 hgemm_status_t hgemm_plan_splitk_range(const hgemm_plan_t* plan, int32_t chunk, int64_t* begin, int64_t* end);
+
+/*
+ * hgemm_plan_splitk_segment -- for a split-K plan, the index-th segment
+ * (0 <= index) that the kernel processes of chunk `chunk`: k-blocks
+ * [*kb0, *kb1) of N tile *tile.  A chunk has one segment per tile its range
+ * touches; they come in ascending order except that the longest (the later
+ * one on a tie) comes last, so the fix-ups of the others finish under its
+ * mainloop.  *first is 1 for the segment that starts the chunk's range (it
+ * decides where the segment's fp32 partial is kept).  INVALID_ARG past the
+ * chunk's last segment or for a bad chunk.
+ */
+hgemm_status_t hgemm_plan_splitk_segment(const hgemm_plan_t* plan, int32_t chunk, int32_t index, int32_t* tile,
+                                         int32_t* kb0, int32_t* kb1, int32_t* first);
 
 /*
  * hgemm_encode_idesc -- the 32-bit tcgen05.mma instruction descriptor the

@@ -218,24 +218,24 @@ hgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int layout, int in, in
     p->cta_group = 1;
     p->tile_m = 128;
     p->tile_n = mma_n;
-    p->block_k = 64;
-    p->stages = splitk_stages_for(mma_n, smem_optin > 0 ? smem_optin : kDefaultSmemOptin);
+    p->block_k = kSplitKBlockK;
+    const int optin = smem_optin > 0 ? smem_optin : kDefaultSmemOptin;
     p->tiles_m = (int32_t)cdiv(N, 128);
     p->tiles_n = 1;
     p->num_tiles = p->tiles_m;
-    p->k_blocks = (int32_t)cdiv(K, 64);
-    const int64_t units = (int64_t)p->num_tiles * p->k_blocks;
-    int64_t grid = num_sms;
-    if (max_ctas > 0 && max_ctas < grid) grid = max_ctas;
-    if (units < grid) grid = units;
-    p->grid = (int32_t)grid;
+    p->k_blocks = (int32_t)cdiv(K, kSplitKBlockK);
+    const SplitKShape sh = splitk_shape(p->num_tiles, p->k_blocks, K, mma_n, num_sms, max_ctas, optin, allow_sk,
+                                        schedule == HGEMM_SCHEDULE_DYNAMIC);
+    p->stages = sh.stages;
+    p->grid = sh.ctas;
     p->group_m = 1;
-    p->smem_bytes = splitk_smem_bytes(mma_n, p->stages);
+    p->smem_bytes = sh.smem_bytes;
     p->tmem_cols = splitk_tmem_cols(mma_n);
-    const SplitChunks ch = splitk_chunks(units, p->grid, schedule == HGEMM_SCHEDULE_DYNAMIC);
+    const SplitChunks ch = sh.chunks;
     p->splitk_chunks = (int32_t)ch.count();
     p->splitk_head_units = ch.head;
-    p->workspace_bytes = (int64_t)splitk_workspace_bytes(ch.count(), mma_n, p->num_tiles);
+    p->splitk_align = ch.align;
+    p->workspace_bytes = ch.align > 1 ? 0 : (int64_t)splitk_workspace_bytes(ch.count(), mma_n, p->num_tiles);
     return HGEMM_OK;
   }
   DenseKind kind = kDense2Sm256;
@@ -431,8 +431,24 @@ hgemm_status_t hgemm_plan_splitk_range(const hgemm_plan_t* plan, int32_t chunk, 
   ch.head = plan->splitk_head_units;
   ch.big = plan->grid;
   ch.n_small = plan->splitk_chunks - plan->grid;
+  ch.align = plan->splitk_align > 1 ? plan->splitk_align : 1;
   *begin = ch.begin(chunk);
   *end = ch.begin((int64_t)chunk + 1);
+  return HGEMM_OK;
+}
+
+hgemm_status_t hgemm_plan_splitk_segment(const hgemm_plan_t* plan, int32_t chunk, int32_t index, int32_t* tile,
+                                         int32_t* kb0, int32_t* kb1, int32_t* first) {
+  int64_t b = 0, e = 0;
+  if (!tile || !kb0 || !kb1 || !first || plan == nullptr || plan->k_blocks <= 0) return HGEMM_ERR_INVALID_ARG;
+  const hgemm_status_t st = hgemm_plan_splitk_range(plan, chunk, &b, &e);
+  if (st != HGEMM_OK) return st;
+  ChunkSegments segs;
+  segs.init(b, e, plan->k_blocks);
+  if (index < 0 || index >= segs.count) return HGEMM_ERR_INVALID_ARG;
+  const int32_t idx = segs.at(index);
+  segs.get(idx, tile, kb0, kb1);
+  *first = idx == 0 ? 1 : 0;
   return HGEMM_OK;
 }
 
@@ -597,7 +613,7 @@ hgemm_status_t hgemm_run(hgemm_handle_t h, const void* A, const void* B, void* C
         !encode_2d(&tmX, in_dtype, A, (uint64_t)K, (uint64_t)M, 64, (uint32_t)mma_n))
       return HGEMM_ERR_CUDA;
     const size_t partial_bytes = (size_t)p.splitk_chunks * 2 * 128 * (size_t)mma_n * sizeof(float);
-    st = ensure_workspace(h, partial_bytes, (size_t)p.num_tiles * 2, s);  // one arrival counter per tile, spare
+    st = ensure_workspace(h, partial_bytes, (size_t)p.num_tiles * kSplitKTicketStride, s);  // one counter per tile
     if (st != HGEMM_OK) return st;
     if ((st = inject_ticket_fault(h, s)) != HGEMM_OK) return st;
     if (p.smem_bytes > h->splitk_prepared_smem) return HGEMM_ERR_UNSUPPORTED;
@@ -612,9 +628,12 @@ hgemm_status_t hgemm_run(hgemm_handle_t h, const void* A, const void* B, void* C
     args.head = p.splitk_head_units;
     args.big = p.grid;
     args.n_small = p.splitk_chunks - p.grid;
+    args.align = p.splitk_align > 1 ? p.splitk_align : 1;
     args.dynamic = h->schedule == HGEMM_SCHEDULE_DYNAMIC ? 1 : 0;
     args.checks = h->checks ? 1 : 0;
     args.stages = p.stages;
+    // the plan's shared memory beyond the ring holds this many prefetched partials
+    args.pf_slots = (p.smem_bytes - splitk_smem_bytes(mma_n, p.stages, 0)) / (128 * mma_n * (int)sizeof(float));
     args.idesc = make_idesc(128, mma_n, in_dtype == HGEMM_BF16, true, false, false);
     args.out_bf16 = out_dtype == HGEMM_BF16;
     args.inject = h->inject;
@@ -622,6 +641,7 @@ hgemm_status_t hgemm_run(hgemm_handle_t h, const void* A, const void* B, void* C
     args.status = h->status;
     args.partials = h->partials;
     args.tickets = h->tickets;
+    args.ticket_stride = kSplitKTicketStride;
     args.C = C;
     args.trace = h->trace;
     // Dynamic schedule: one CTA per chunk; the CTAs that run take over the rest.

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "sched.cuh"
+
 namespace hg {
 
 // Device status word layout (shared with hgemm_sync_status).
@@ -29,7 +31,7 @@ enum TraceKind : uint16_t {
   kTraceKernelEnd = 2,      // before teardown (value: SM clock counter, low 31 bits)
   kTraceItemBegin = 3,      // a role starts a work item (value: first k-block, or slot for the epilogue)
   kTraceItemEnd = 4,        // a role finishes it
-  kTracePartialStored = 5,  // stream-K partial published (value: ticket drawn)
+  kTracePartialStored = 5,  // stream-K / split-K partial published (value: ticket drawn)
   kTraceReduced = 6,        // a split tile reduced and stored (value: contributors)
   kTraceStall = 7,          // SM cycles the role spent blocked on barriers during the item
 };
@@ -89,29 +91,53 @@ struct SplitKArgs {
   int32_t M, N, K;
   int32_t mma_n;     // M rounded up to a multiple of 16 (the MMA's N)
   int32_t n_tiles;   // ceil(N / 128)
-  int32_t k_blocks;  // ceil(K / 64)
+  int32_t k_blocks;  // ceil(K / kSplitKBlockK)
   int64_t units;     // n_tiles * k_blocks
   int64_t head;      // units covered by the first `big` chunks (all units under the static schedule)
   int32_t big;       // big chunks (= CTAs of the static schedule)
   int32_t n_small;   // small chunks after them (dynamic schedule), else 0
+  int32_t align;     // big chunks cut in steps of this many units: k_blocks (whole tiles) or 1
   int32_t dynamic;   // 1: one CTA per chunk, chunks taken over by cluster launch control
   int32_t checks;    // 1: check invariants, report violations as kStatusCheck
   int32_t stages;
+  int32_t pf_slots;  // partials that fit in the shared-memory prefetch area (splitk_pf_slots)
   uint32_t idesc;
   int32_t out_bf16;
   int32_t inject;
   uint64_t timeout_ns;
   int32_t* status;
   float* partials;   // [big + n_small chunks][2][128][mma_n] fp32
-  int32_t* tickets;  // [n_tiles] arrival counters (space for 2 x n_tiles); all zero between launches
+  int32_t* tickets;  // arrival counters, tile t's at tickets[t * ticket_stride]; all zero between launches
+  int32_t ticket_stride;  // int32 words between counters: kSplitKTicketStride (one 128-byte line each), or 1
   void* C;           // [M][N] row-major
   TraceBuf* trace;   // null unless tracing
 };
 
 constexpr int kSplitKMaxM = 64;
+constexpr int kSplitKBlockK = 128;  // K per pipeline stage (and per work unit)
+// Split-K arrival counters, one per 128-byte line: a counter is polled by its
+// tile's last contributor while the others draw tickets on it, and counters
+// packed 32 to a line made every such access queue behind those of 31 other
+// tiles.
+constexpr int kSplitKTicketStride = 32;
+// The last contributor of a split tile copies up to this many other partials
+// into shared memory ahead of its sum.
+constexpr int kSplitKMaxPrefetch = 4;
 int splitk_stage_bytes(int mma_n);
-int splitk_smem_bytes(int mma_n, int stages);
-int splitk_stages_for(int mma_n, int smem_optin);
+int splitk_pf_slots(int mma_n, int stages, int smem_optin);
+int splitk_smem_bytes(int mma_n, int stages, int pf_slots);
+int splitk_stages_for(int mma_n, int smem_optin, int most);
+
+// How a skinny product is laid out over the CTAs (splitk_shape).
+struct SplitKShape {
+  SplitChunks chunks;  // the work ids; chunks.align > 1: whole tiles, no fix-up
+  int32_t ctas;        // CTAs launched (static schedule) / running at most (dynamic)
+  int32_t stages, pf_slots, smem_bytes;
+};
+// split_k: 0 never splits a tile's K range between CTAs, 2 always does, 1
+// decides by the estimate in gemm_splitk.cu.  max_ctas > 0 caps the CTAs.
+SplitKShape splitk_shape(int64_t tiles, int32_t k_blocks, int64_t K, int mma_n, int num_sms, int max_ctas,
+                         int smem_optin, int split_k, bool dynamic);
 int splitk_tmem_cols(int mma_n);
 size_t splitk_workspace_bytes(int64_t chunks, int mma_n, int n_tiles);
 cudaError_t splitk_prepare(int smem_bytes);

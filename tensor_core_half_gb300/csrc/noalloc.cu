@@ -29,7 +29,7 @@ namespace {
 // Scratch layout: [status word | per-tile tickets | fp32 partial sums].
 constexpr size_t kNoAllocScratchBytes = (size_t)16 << 20;  // 16 MiB
 constexpr size_t kStatusBytes = 256;
-constexpr size_t kTicketBytes = (size_t)2 << 20;  // 2 counters x 262144 tiles: N <= 33,554,432
+constexpr size_t kTicketBytes = (size_t)2 << 20;  // N <= 33,554,432; one counter per line up to 16384 tiles
 constexpr size_t kPartialOffset = kStatusBytes + kTicketBytes;
 constexpr size_t kPartialBytes = kNoAllocScratchBytes - kPartialOffset;
 constexpr int kMaxDevices = 64;
@@ -142,17 +142,19 @@ extern "C" hgemm_status_t hgemm_run_splitk_noalloc(const void* A, const void* B,
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (K == 0) return hg::fill_zero_launch(C, c_bytes, s) == cudaSuccess ? HGEMM_OK : HGEMM_ERR_CUDA;
 
-  // Plan: the same balanced split as hgemm_run's split-K variant, with the CTA
-  // count capped so the partial sums fit the scratch.
+  // Plan: the same layout as hgemm_run's split-K variant (whole tiles or the
+  // balanced split), with the CTA count capped so the partial sums fit the
+  // scratch.
   const int mma_n = (int)((M + 15) / 16) * 16;
-  const int stages = hg::splitk_stages_for(mma_n, d->smem_optin);
-  const int smem = hg::splitk_smem_bytes(mma_n, stages);
-  const int64_t k_blocks = (K + 63) / 64;
-  const int64_t units = n_tiles * k_blocks;
+  const int64_t k_blocks = (K + hg::kSplitKBlockK - 1) / hg::kSplitKBlockK;
   const size_t per_cta = (size_t)2 * 128 * (size_t)mma_n * sizeof(float);
-  int64_t grid = d->sm_count;
-  if ((int64_t)(kPartialBytes / per_cta) < grid) grid = (int64_t)(kPartialBytes / per_cta);
-  if (units < grid) grid = units;
+  const hg::SplitKShape sh = hg::splitk_shape(n_tiles, (int32_t)k_blocks, K, mma_n, d->sm_count,
+                                              (int)(kPartialBytes / per_cta), d->smem_optin, 1, false);
+  const int64_t units = n_tiles * k_blocks;
+  const int64_t grid = sh.ctas;
+  const int stages = sh.stages;
+  const int pf_slots = sh.pf_slots;
+  const int smem = sh.smem_bytes;
 
   CUtensorMap tmW, tmX;
   if (!encode(&tmW, in_dtype, B, (uint64_t)K, (uint64_t)N, 64, 128) ||
@@ -161,7 +163,11 @@ extern "C" hgemm_status_t hgemm_run_splitk_noalloc(const void* A, const void* B,
 
   // The array keeps whatever the previous call left: clear the status word and
   // the tickets this call uses (they must start at zero), on the same stream.
-  const size_t clear = (kStatusBytes + (size_t)n_tiles * 2 * sizeof(int32_t) + 15) & ~(size_t)15;
+  // One counter per 128-byte line where they fit, else packed.
+  const int32_t stride = ((size_t)n_tiles * hg::kSplitKTicketStride * sizeof(int32_t) <= kTicketBytes)
+                             ? hg::kSplitKTicketStride
+                             : 1;
+  const size_t clear = (kStatusBytes + (size_t)n_tiles * stride * sizeof(int32_t) + 15) & ~(size_t)15;
   if (hg::fill_zero_launch(d->scratch, clear, s) != cudaSuccess) return HGEMM_ERR_CUDA;
 
   hg::SplitKArgs args;
@@ -172,18 +178,21 @@ extern "C" hgemm_status_t hgemm_run_splitk_noalloc(const void* A, const void* B,
   args.n_tiles = (int32_t)n_tiles;
   args.k_blocks = (int32_t)k_blocks;
   args.units = units;
-  args.head = units;  // the static split: one equal range per CTA
+  args.head = sh.chunks.head;  // static: one range per CTA
   args.big = (int32_t)grid;
   args.n_small = 0;
+  args.align = sh.chunks.align;
   args.dynamic = 0;
   args.checks = 0;
   args.stages = stages;
+  args.pf_slots = pf_slots;
   args.idesc = hg::make_idesc(128, mma_n, in_dtype == HGEMM_BF16, true, false, false);
   args.out_bf16 = out_dtype == HGEMM_BF16;
   args.inject = 0;
   args.timeout_ns = hg::kDefaultTimeoutNs;
   args.status = reinterpret_cast<int32_t*>(d->scratch);
   args.tickets = reinterpret_cast<int32_t*>(d->scratch + kStatusBytes);
+  args.ticket_stride = stride;
   args.partials = reinterpret_cast<float*>(d->scratch + kPartialOffset);
   args.C = C;
   args.trace = nullptr;

@@ -137,6 +137,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Same, suspending the thread for up to about `hint_ns` while the phase is
+// incomplete (it resumes as soon as the phase completes).
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.b32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Same, with cluster-scope acquire: pairs with releases from the peer CTA
 // (remote arrivals, multicast tcgen05.commit).
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
@@ -408,6 +422,16 @@ __device__ __forceinline__ int32_t ld_acquire_gpu(const int32_t* p) {
   return v;
 }
 
+// A morally strong load with no ordering of its own (polling); pair it with
+// fence_acq_rel_gpu once the value seen calls for acquire semantics.
+__device__ __forceinline__ int32_t ld_relaxed_gpu(const int32_t* p) {
+  int32_t v;
+  asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 // Add with release semantics at GPU scope: the writes that happen before it
 // (including other threads' writes ordered by a CTA barrier) become visible to
 // a thread that acquires the new value.
@@ -435,6 +459,15 @@ static __device__ __noinline__ bool wait_counter_geq(const int32_t* p, int32_t t
     }
   }
 }
+
+// ------------------------------------------------------ per-thread async ----
+// 16-byte global -> shared copy issued by this thread (L2 only), completed by
+// cp_async_wait_all in the same thread.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 // ------------------------------------------------------------ tracing ----
 // Appends one event to a trace buffer (see kernels.h); no-op for a null buffer.

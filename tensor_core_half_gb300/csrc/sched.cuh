@@ -52,18 +52,21 @@ HG_HD int64_t splitk_owner(int64_t u, int64_t units, int64_t ctas) { return ((u 
 // schedule: about three quarters of the units in one big chunk per SM, the
 // rest in small chunks that the SMs which finish first take over, so that
 // work still spreads when some SMs are busy with other kernels.
+// align > 1 (whole-tile split, align = k_blocks): the big chunks cut the
+// head in steps of `align` units, so that every chunk is whole tiles.
 struct SplitChunks {
   int64_t units, head;
   int32_t big, n_small;
+  int32_t align = 1;
 
   HG_HD int64_t count() const { return (int64_t)big + n_small; }
   HG_HD int64_t begin(int64_t g) const {
-    if (g <= big) return splitk_begin(g, head, big);
+    if (g <= big) return align * splitk_begin(g, head / align, big);
     return head + splitk_begin(g - big, units - head, n_small);
   }
   // The chunk that holds unit u.
   HG_HD int64_t owner(int64_t u) const {
-    if (u < head) return splitk_owner(u, head, big);
+    if (u < head) return splitk_owner(u / align, head / align, big);
     return big + splitk_owner(u - head, units - head, n_small);
   }
 };
@@ -87,6 +90,61 @@ HG_HD SplitChunks splitk_chunks(int64_t units, int32_t ctas, bool dynamic) {
     c.head = units - tail;
     c.n_small = (int32_t)((tail + size - 1) / size);
   }
+  return c;
+}
+
+// The segments of a split-K chunk [begin, end): one per N tile it touches,
+// k-blocks [kb0, kb1) of that tile.  They are processed in ascending order,
+// except that the longest (the later one on a tie) goes last.  A segment's
+// fix-up runs in the epilogue after its MMAs, one segment after another, so a
+// short segment at the end of a chunk would wait behind the fix-up of the
+// long one before it and both would end the kernel; with the long segment
+// last, the other fix-ups finish under its mainloop.  Where a segment sits in
+// K (first of its chunk or not) still decides where its partial is kept.
+struct ChunkSegments {
+  int64_t begin, end, tile_lo;
+  int32_t k_blocks, count, longest;
+
+  HG_HD void init(int64_t b, int64_t e, int32_t kb) {
+    begin = b;
+    end = e;
+    k_blocks = kb;
+    tile_lo = b / kb;
+    count = (e > b) ? (int32_t)((e - 1) / kb - tile_lo + 1) : 0;
+    longest = 0;
+    if (count >= 2) {
+      int64_t best = (tile_lo + 1) * kb - b;  // segment 0
+      if (count >= 3 && kb >= best) {         // the last whole tile in between
+        longest = count - 2;
+        best = kb;
+      }
+      if (e - (tile_lo + count - 1) * kb >= best) longest = count - 1;
+    }
+  }
+  // Segment index processed at position i (0 <= i < count).
+  HG_HD int32_t at(int32_t i) const {
+    if (i < longest) return i;
+    return (i + 1 < count) ? i + 1 : longest;
+  }
+  HG_HD void get(int32_t idx, int32_t* tile, int32_t* kb0, int32_t* kb1) const {
+    const int64_t t = tile_lo + idx;
+    const int64_t lo = (idx == 0) ? begin : t * k_blocks;
+    const int64_t hi = (t + 1) * k_blocks < end ? (t + 1) * k_blocks : end;
+    *tile = (int32_t)t;
+    *kb0 = (int32_t)(lo - t * k_blocks);
+    *kb1 = (int32_t)(hi - t * k_blocks);
+  }
+};
+
+// Whole tiles, none split along K: CTA c of `ctas` takes tiles
+// [floor(c T / ctas), floor((c+1) T / ctas)).
+HG_HD SplitChunks splitk_whole_tiles(int64_t tiles, int32_t k_blocks, int32_t ctas) {
+  SplitChunks c;
+  c.units = tiles * k_blocks;
+  c.head = c.units;
+  c.big = ctas;
+  c.n_small = 0;
+  c.align = k_blocks;
   return c;
 }
 

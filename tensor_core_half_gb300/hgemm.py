@@ -82,7 +82,8 @@ class hgemm_plan_t(ctypes.Structure):
         "k_blocks", "grid", "group_m", "smem_bytes", "tmem_cols")] + [
         ("workspace_bytes", ctypes.c_int64), ("dp_tiles", ctypes.c_int32), ("stream_k", ctypes.c_int32),
         ("sk_units", ctypes.c_int64), ("sk_ranges", ctypes.c_int32), ("work_ids", ctypes.c_int32),
-        ("schedule", ctypes.c_int32), ("splitk_chunks", ctypes.c_int32), ("splitk_head_units", ctypes.c_int64)]
+        ("schedule", ctypes.c_int32), ("splitk_chunks", ctypes.c_int32), ("splitk_head_units", ctypes.c_int64),
+        ("splitk_align", ctypes.c_int32)]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -126,6 +127,8 @@ _lib.hgemm_plan_tile.argtypes = [ctypes.POINTER(hgemm_plan_t), _i32, ctypes.POIN
 _lib.hgemm_plan_splitk_range.restype = _i32
 _lib.hgemm_plan_splitk_range.argtypes = [ctypes.POINTER(hgemm_plan_t), _i32, ctypes.POINTER(_i64),
                                          ctypes.POINTER(_i64)]
+_lib.hgemm_plan_splitk_segment.restype = _i32
+_lib.hgemm_plan_splitk_segment.argtypes = [ctypes.POINTER(hgemm_plan_t), _i32, _i32] + [ctypes.POINTER(_i32)] * 4
 _lib.hgemm_encode_idesc.restype = _u32
 _lib.hgemm_encode_idesc.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32]
 _lib.hgemm_encode_smem_desc.restype = _u64
@@ -284,6 +287,13 @@ def hgemm_plan_splitk_range(plan, cta):
     b, e = _i64(), _i64()
     st = _lib.hgemm_plan_splitk_range(ctypes.byref(plan), int(cta), ctypes.byref(b), ctypes.byref(e))
     return int(st), b.value, e.value
+
+
+def hgemm_plan_splitk_segment(plan, chunk, index):
+    t, k0, k1, f = _i32(), _i32(), _i32(), _i32()
+    st = _lib.hgemm_plan_splitk_segment(ctypes.byref(plan), int(chunk), int(index), ctypes.byref(t), ctypes.byref(k0),
+                                        ctypes.byref(k1), ctypes.byref(f))
+    return int(st), t.value, k0.value, k1.value, f.value
 
 
 def hgemm_encode_idesc(mma_m, mma_n, in_dtype, acc_dtype, a_mn_major=0, b_mn_major=0) -> int:

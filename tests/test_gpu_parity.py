@@ -127,6 +127,29 @@ def test_splitk_shapes(h, M, N, K):
     parity.check(got, ab, bb, M, N, K, "TN", "bf16", "f32", "bf16")
 
 
+@pytest.mark.parametrize("stream_k", [0, 1, 2], ids=["whole", "auto", "split"])
+@pytest.mark.parametrize("M,N,K", [(16, 16384, 2048), (33, 12288, 1024), (64, 20480, 520), (1, 8, 64),
+                                   (5, 1000, 72), (48, 2048, 4104)])
+def test_splitk_layouts(h, M, N, K, stream_k):
+    # Whole tiles per CTA (no tile's K range split: no partials, no fix-up)
+    # and the balanced K split give the same products up to fp32 summation
+    # order; HGEMM_OPT_STREAM_K 0 / 2 force one or the other.
+    a, b, ab, bb = parity.inputs(M, N, K, "TN", "bf16", ("normal", 1.0), 91)
+    got = run(h, a, b, M, N, K, "TN", "f32", "bf16", "splitk", stream_k=stream_k)
+    parity.check(got, ab, bb, M, N, K, "TN", "bf16", "f32", "bf16")
+    again = run(h, a, b, M, N, K, "TN", "f32", "bf16", "splitk", stream_k=stream_k)
+    assert np.array_equal(got, again)
+
+
+@pytest.mark.parametrize("stream_k", [0, 2], ids=["whole", "split"])
+def test_splitk_layouts_small_integers_bit_exact(h, stream_k):
+    M, N, K = 24, 16384, 4096
+    a, b, ab, bb = parity.inputs(M, N, K, "TN", "bf16", ("int", -4, 4), 92)
+    got = run(h, a, b, M, N, K, "TN", "f32", "bf16", "splitk", stream_k=stream_k)
+    ref, _, _ = oracle.gemm(ab, bb, M, N, K, "TN", "bf16", "bf16")
+    assert np.array_equal(got, ref)
+
+
 @pytest.mark.parametrize("M", [1, 16, 33, 64])
 @pytest.mark.parametrize("N,K", [(4096, 1024), (384, 8192), (16384, 2048), (1000, 4104)])
 def test_splitk_dynamic_parity(h, M, N, K):
@@ -370,7 +393,8 @@ def test_bounded_wait_gives_up_and_recovers(h, variant, M, schedule):
 CHECKED_CASES = [("2sm256", "TN", 4096, 4096, 256, 2, "static"), ("2sm256", "TN", 4096, 4096, 256, 2, "dynamic"),
                  ("1sm128", "NN", 1000, 3000, 520, 1, "dynamic"), ("2sm192", "TN", 1000, 3000, 4104, 1, "static"),
                  ("1sm256", "TN", 2048, 4096, 192, 1, "dynamic"), ("2sm256", "NN", 768, 520, 4104, 1, "static"),
-                 ("splitk", "TN", 16, 16384, 4096, 1, "static"), ("splitk", "TN", 40, 8192, 8192, 1, "dynamic")]
+                 ("splitk", "TN", 16, 16384, 4096, 1, "static"), ("splitk", "TN", 16, 16384, 4096, 2, "static"),
+                 ("splitk", "TN", 40, 8192, 8192, 1, "dynamic")]
 
 
 @pytest.mark.parametrize("variant,layout,M,N,K,sk,schedule", CHECKED_CASES)

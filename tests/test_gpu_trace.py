@@ -135,3 +135,35 @@ def test_dynamic_splitk_takes_over_small_chunks():
             for kb in range(sp["begin_value"], sp["end_value"]):
                 covered[(sp["tile"], kb)] += 1
     assert len(covered) == p.num_tiles * p.k_blocks and set(covered.values()) == {1}
+
+
+@pytest.mark.parametrize("M,N,K", [(16, 16384, 8192), (16, 4096, 4096), (48, 3000, 2000)])
+def test_splitk_segments_in_plan_order(M, N, K):
+    """Static split-K: every CTA's MMA issuer works through its chunk's
+    segments in the order the planner gives (longest last)."""
+    with hgemm.Handle() as h:
+        h.set_option(hgemm.HGEMM_OPT_TRACE, 1 << 18)
+        a, b, _, _ = parity.inputs(M, N, K, "TN", "bf16", ("normal", 1.0), 75)
+        A, B = a.cuda(), b.cuda()
+        C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        h.run(A, B, C, layout="TN", acc="f32")
+        assert h.sync_status()[0] == hgemm.HGEMM_OK
+        st, n, rows = hgemm.hgemm_trace_read(h.h, 1 << 18)
+        assert st == hgemm.HGEMM_OK and n == len(rows) > 0
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    st, p = hgemm.hgemm_plan(M, N, K, num_sms=sms)
+    assert p.variant == hgemm.HGEMM_VARIANT_SPLITK
+    seen = collections.defaultdict(list)
+    for t, cta, role, kind, item, value in sorted(rows):
+        if role == 2 and kind == 3:
+            seen[cta].append((item, value))
+    assert len(seen) == p.grid
+    for c in range(p.grid):
+        expect, i = [], 0
+        while True:
+            s, tile, kb0, kb1, first = hgemm.hgemm_plan_splitk_segment(p, c, i)
+            if s != hgemm.HGEMM_OK:
+                break
+            expect.append((tile, kb0))
+            i += 1
+        assert seen[c] == expect, c

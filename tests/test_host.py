@@ -80,7 +80,10 @@ def test_plan_variant_choice():
     assert st == ST_OK and p.variant == H.HGEMM_VARIANT_2SM_256x256 and p.stream_k == 0
     st, p = plan(16, 16384, 8192)
     assert st == ST_OK and p.variant == H.HGEMM_VARIANT_SPLITK and p.tile_n == 16 and p.num_tiles == 128
-    assert p.grid == 152 and p.k_blocks == 128 and p.workspace_bytes > 0
+    # whole tiles: one 128-row tile per CTA on 128 of the 152 SMs, no partials
+    assert p.grid == 128 and p.block_k == 128 and p.k_blocks == 64 and p.splitk_align == 64 and p.workspace_bytes == 0
+    st, p = plan(16, 16384, 8192, stream_k=2)
+    assert st == ST_OK and p.grid == 152 and p.splitk_align == 1 and p.workspace_bytes > 0
     st, p = plan(16, 16384, 8192, layout=H.HGEMM_LAYOUT_NN)
     assert st == ST_OK and p.variant != H.HGEMM_VARIANT_SPLITK  # split-K is TN only
     st, p = plan(16, 16384, 8192, fin=0, acc=0, out=0)
@@ -139,11 +142,74 @@ def test_splitk_partition(M, N, K, sms):
     for c in range(p.grid):
         s, b, e = H.hgemm_plan_splitk_range(p, c)
         assert s == ST_OK and b == prev_end and e > b
+        if p.splitk_align > 1:  # whole tiles: ranges start and end on tile boundaries
+            assert p.splitk_align == p.k_blocks and b % p.k_blocks == 0 and e % p.k_blocks == 0
         sizes.append(e - b)
         prev_end = e
     assert prev_end == units
-    assert max(sizes) - min(sizes) <= 1
+    assert max(sizes) - min(sizes) <= max(1, p.splitk_align)
     assert H.hgemm_plan_splitk_range(p, p.grid)[0] == ST_INV
+
+
+@pytest.mark.parametrize("M,N,K,sms,whole,grid", [
+    (16, 16384, 8192, 152, True, 128),    # 128 tiles: one per CTA, 24 SMs idle, HBM still saturated
+    (16, 32768, 4096, 152, True, 128),    # 256 tiles: two per CTA
+    (16, 12288, 8192, 152, True, 96),     # 96 CTAs reach ~5.9 of 6.25 TB/s: still ahead of split + fix-up
+    (16, 8192, 8192, 152, False, 152),    # 64 CTAs would reach ~4 TB/s: split over every SM
+    (16, 20480, 8192, 152, False, 152),   # 160 tiles -> 80 CTAs of two tiles: too few
+    (16, 4096, 4096, 152, False, 152),
+    (16, 16384, 8192, 148, True, 128)])
+def test_splitk_whole_tile_choice(M, N, K, sms, whole, grid):
+    """The planner's layout for skinny products: whole tiles per CTA (no
+    tile's K range split, no fix-up) when 128-row tiles at the CTA count that
+    takes them saturate HBM about as well as all SMs, else the balanced split;
+    HGEMM_OPT_STREAM_K 0 / 2 force one or the other."""
+    st, p = plan(M, N, K, sms=sms)
+    assert st == ST_OK and p.variant == H.HGEMM_VARIANT_SPLITK
+    assert (p.splitk_align == p.k_blocks) == whole and p.grid == grid
+    assert (p.workspace_bytes == 0) == whole
+    st, p0 = plan(M, N, K, sms=sms, stream_k=0)
+    per = -(-p0.num_tiles // sms)
+    assert p0.splitk_align == p0.k_blocks and p0.grid == -(-p0.num_tiles // per) and p0.workspace_bytes == 0
+    st, p2 = plan(M, N, K, sms=sms, stream_k=2)
+    assert p2.splitk_align == 1 and p2.grid == min(sms, p2.num_tiles * p2.k_blocks)
+    st, pd = H.hgemm_plan(M, N, K, num_sms=sms, schedule=H.HGEMM_SCHEDULE_DYNAMIC)
+    assert pd.splitk_align == 1  # the dynamic schedule always splits
+
+
+@pytest.mark.parametrize("schedule", [H.HGEMM_SCHEDULE_STATIC, H.HGEMM_SCHEDULE_DYNAMIC])
+@pytest.mark.parametrize("M,N,K,sms", [(16, 16384, 8192, 152), (1, 8, 64, 152), (64, 1000, 72, 148),
+                                       (16, 4096, 4096, 7), (33, 100000, 640, 152), (16, 128, 8192, 152)])
+def test_splitk_segment_order(M, N, K, sms, schedule):
+    """The segments a chunk is processed in: one per N tile its range touches
+    (found here by walking the chunk unit by unit), all of them once, the
+    longest last (the later one on a tie), the rest in ascending order, and
+    'first' on the one that starts the range."""
+    st, p = H.hgemm_plan(M, N, K, num_sms=sms, schedule=schedule)
+    assert st == ST_OK and p.variant == H.HGEMM_VARIANT_SPLITK
+    kb = p.k_blocks
+    for g in range(p.splitk_chunks):
+        s, b, e = H.hgemm_plan_splitk_range(p, g)
+        assert s == ST_OK
+        pieces = {}
+        for u in range(b, e):
+            t, k = divmod(u, kb)
+            lo, hi = pieces.get(t, (k, k))
+            pieces[t] = (min(lo, k), max(hi, k + 1))
+        expect = [(t,) + pieces[t] for t in sorted(pieces)]
+        got = []
+        for i in range(len(expect)):
+            s, t, k0, k1, first = H.hgemm_plan_splitk_segment(p, g, i)
+            assert s == ST_OK
+            assert first == (t * kb + k0 == b)
+            got.append((t, k0, k1))
+        assert H.hgemm_plan_splitk_segment(p, g, len(expect))[0] == ST_INV
+        assert sorted(got) == expect
+        lengths = [x[2] - x[1] for x in expect]
+        longest = max(i for i, n in enumerate(lengths) if n == max(lengths))
+        assert got == expect[:longest] + expect[longest + 1:] + [expect[longest]]
+    assert H.hgemm_plan_splitk_segment(p, p.splitk_chunks, 0)[0] == ST_INV
+    assert H.hgemm_plan_splitk_segment(p, 0, -1)[0] == ST_INV
 
 
 @pytest.mark.parametrize("M,N,K,sms", [(16, 16384, 8192, 152), (1, 8, 64, 152), (64, 1000, 72, 148),
@@ -172,9 +238,9 @@ def test_splitk_dynamic_chunks(M, N, K, sms):
         assert max(small) <= max(1, units // (p.grid * 4)) + 1
     else:
         assert not small and p.splitk_head_units == units  # too little work to split further
-    # the static plan of the same problem: one range per CTA
-    st, q = H.hgemm_plan(M, N, K, num_sms=sms, schedule=H.HGEMM_SCHEDULE_STATIC)
-    assert q.splitk_chunks == q.grid == p.grid and q.splitk_head_units == units
+    # the static plan of the same problem split over every SM: one range per CTA
+    st, q = H.hgemm_plan(M, N, K, num_sms=sms, stream_k=2, schedule=H.HGEMM_SCHEDULE_STATIC)
+    assert q.splitk_chunks == q.grid == p.grid and q.splitk_head_units == units and q.splitk_align == 1
 
 
 # ------------------------------------------------------------ descriptors ----
