@@ -416,7 +416,7 @@ typedef struct {
   int32_t mode;       /* hgemm_tma_mode_t                                                    */
   int32_t tile_rows;  /* 8..256, a multiple of 8                                              */
   int32_t tile_cols;  /* a multiple of 8 (of 64 for the 128-byte modes; <= 2048 for 3D_16B)   */
-  int32_t depth;      /* tiles in flight per CTA (shared-memory slots), 1..8                  */
+  int32_t depth;      /* tiles in flight per CTA (shared-memory slots), 1..16                 */
   int32_t issuers;    /* warps issuing a tile's copies, 1 or 2 (<= copies per tile)           */
   int32_t ctas;       /* CTAs, one per SM; 0 = every SM                                       */
   int32_t iters;      /* tiles each CTA copies                                                */

@@ -36,7 +36,7 @@ namespace hg {
 namespace {
 
 constexpr int kBenchThreads = 128;
-constexpr int kMaxDepth = 8;
+constexpr int kMaxDepth = 16;
 
 struct BenchArgs {
   int32_t mode, tile_rows, tile_cols, depth, issuers, iters, walk;

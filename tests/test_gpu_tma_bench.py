@@ -47,7 +47,7 @@ def test_rejects_bad_shapes(src):
     bad = [(hgemm.HGEMM_TMA_2D_128B, 128, 96, 2, 8, 1),   # 128-byte modes need 64-column multiples
            (hgemm.HGEMM_TMA_2D_16B, 100, 64, 2, 8, 1),    # rows multiple of 8
            (hgemm.HGEMM_TMA_3D_16B, 128, 64, 2, 8, 2),    # one copy per tile: one issuer
-           (hgemm.HGEMM_TMA_2D_128B, 128, 64, 9, 8, 1),   # depth <= 8
+           (hgemm.HGEMM_TMA_2D_128B, 128, 64, 17, 8, 1),  # depth <= 16
            (7, 128, 64, 2, 8, 1)]
     st = hgemm.hgemm_tma_bench(src.data_ptr(), h, w, hgemm.HGEMM_TMA_BULK, 128, 64, 2, 8, walk=2)[0]
     assert st == hgemm.HGEMM_ERR_INVALID_ARG
