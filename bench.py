@@ -517,7 +517,8 @@ def sweep(args):
                            "plan": {"variant": list(hgemm.VARIANTS)[plan.variant], "grid": plan.grid,
                                     "tile": [plan.tile_m, plan.tile_n], "stages": plan.stages,
                                     "stream_k": bool(plan.stream_k), "work_ids": plan.work_ids,
-                                    "splitk_chunks": plan.splitk_chunks},
+                                    "splitk_chunks": plan.splitk_chunks,
+                                    "splitk_whole_tiles": plan.splitk_align > 1},
                            "gpu": props.name, "sms": props.multi_processor_count,
                            "clocks": sampler.summary(h0, h1)}
                 h.close()
