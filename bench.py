@@ -215,6 +215,60 @@ def cpu_oracle_sample(w, a_bits, b_bits, target_s: float):
         rows = min(w.M, max(rows * 2, int(rows * target_s / max(dt, 1e-3) * 1.1)))
 
 
+def host_cpu_model() -> str:
+    """The host CPU: lscpu's model name, else /proc/cpuinfo's (or the Arm part number)."""
+    try:
+        import subprocess
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read().splitlines()
+    except OSError:
+        return "unknown"
+    for key in ("model name", "Model name", "Hardware"):
+        for line in info:
+            if line.startswith(key) and ":" in line:
+                return line.split(":", 1)[1].strip()
+    impl = [l.split(":", 1)[1].strip() for l in info if l.startswith("CPU implementer")]
+    part = [l.split(":", 1)[1].strip() for l in info if l.startswith("CPU part")]
+    return "CPU implementer %s, part %s" % (impl[0] if impl else "?", part[0] if part else "?")
+
+
+def oracle_timing():
+    """The CPU oracle on the small workloads, one thread and all host cores:
+    each a median of 3 full products (one run where a single-threaded product
+    takes over 30 s), GFLOP/s = 2MNK / t.  One JSON line per run."""
+    import numpy as np
+
+    import oracle
+    from tensor_core_half_gb300 import workloads
+    cores = os.cpu_count() or 1
+    nproc = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else cores
+    model = host_cpu_model()
+    for name in ("square256_f16", "sweep2048_f16_accf32"):
+        w = workloads.WORKLOADS[name]
+        a, b = workloads.generate_workload(w)
+        ab, bb = workloads.bits(a), workloads.bits(b)
+        for threads in (1, nproc):
+            times = []
+            for _ in range(3):
+                t0 = time.perf_counter()
+                oracle.gemm(ab, bb, w.M, w.N, w.K, w.layout, w.in_dtype, w.out_dtype, nthreads=threads)
+                times.append(time.perf_counter() - t0)
+                if times[-1] > 30.0:
+                    break
+            t = float(np.median(times))
+            print(json.dumps({"oracle_timing": name, "M": w.M, "N": w.N, "K": w.K, "in": w.in_dtype,
+                              "threads": threads, "runs": len(times), "seconds": round(t, 4),
+                              "gflops": round(2.0 * w.M * w.N * w.K / t / 1e9, 3), "hardware_concurrency": cores,
+                              "nproc": nproc, "cpu": model}), flush=True)
+
+
 # ------------------------------------------------------------------ main ----
 def main():
     ap = argparse.ArgumentParser()
@@ -231,6 +285,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--oracle-timing", action="store_true",
+                    help="time the CPU oracle on the 256^3 and 2048^3 workloads, one thread and all cores")
     ap.add_argument("--sweep", default=None, metavar="JSONL",
                     help="measure every workload of the table (and --sweep-variants, --sweep-schedules), one JSON "
                          "record per line appended to JSONL; records already there are skipped, so an "
@@ -240,6 +296,9 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.oracle_timing:
+        oracle_timing()
+        return
     if args.sweep:
         sweep(args)
         return
