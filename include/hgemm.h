@@ -158,6 +158,9 @@ typedef struct {
  * The device must be compute capability 10.3 (sm_103).  Allocates a 16-byte
  * device status word.  Returns NO_DEVICE when no device/driver is usable,
  * UNSUPPORTED for another architecture, CUDA on any other CUDA failure.
+ * For tests, the environment variable HGEMM_FORCE_VARIANT (auto, 1sm128,
+ * 1sm256, 2sm256, splitk, 2sm192, or the hgemm_variant_t number) sets the new
+ * handle's HGEMM_OPT_FORCE_VARIANT; unset or unrecognised means automatic.
  */
 hgemm_status_t hgemm_create(hgemm_handle_t* out);
 

@@ -11,6 +11,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <algorithm>
@@ -83,6 +84,21 @@ void load_encode() {
 }
 
 bool valid_dtype(int d) { return d == HGEMM_F16 || d == HGEMM_BF16 || d == HGEMM_F32; }
+
+// Test-only pin of the variant for every new handle: HGEMM_FORCE_VARIANT =
+// auto | 1sm128 | 1sm256 | 2sm256 | splitk | 2sm192, or the hgemm_variant_t
+// number.  Unset or unrecognised: automatic choice (HGEMM_VARIANT_AUTO).
+int env_force_variant() {
+  const char* v = getenv("HGEMM_FORCE_VARIANT");
+  if (v == nullptr || *v == 0) return HGEMM_VARIANT_AUTO;
+  static const struct { const char* name; int id; } names[] = {
+      {"auto", HGEMM_VARIANT_AUTO},        {"1sm128", HGEMM_VARIANT_1SM_128x128}, {"1sm256", HGEMM_VARIANT_1SM_128x256},
+      {"2sm256", HGEMM_VARIANT_2SM_256x256}, {"splitk", HGEMM_VARIANT_SPLITK},    {"2sm192", HGEMM_VARIANT_2SM_256x192}};
+  for (const auto& n : names)
+    if (strcmp(v, n.name) == 0) return n.id;
+  if (v[0] >= '0' && v[0] <= '5' && v[1] == 0) return v[0] - '0';
+  return HGEMM_VARIANT_AUTO;
+}
 
 // Checks that do not involve pointers.  Order: sizes, enums, combinations, pitches.
 hgemm_status_t check_problem(int64_t M, int64_t N, int64_t K, int layout, int in, int acc, int out) {
@@ -488,6 +504,7 @@ hgemm_status_t hgemm_create(hgemm_handle_t* out) {
     delete c;
     return cuda_status(e);
   }
+  c->force_variant = env_force_variant();
   *out = c;
   return HGEMM_OK;
 }

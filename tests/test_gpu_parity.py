@@ -469,3 +469,23 @@ def test_run_host_back_to_back_calls(h):
     assert h.sync_status()[0] == hgemm.HGEMM_OK
     for (a, b, ab, bb), C in zip(sets, outs):
         parity.check(workloads.bits(C), ab, bb, M, N, K, "TN", "f16", "f32", "f16")
+
+
+def test_env_force_variant(monkeypatch):
+    # HGEMM_FORCE_VARIANT pins the variant of the handles created while it is
+    # set: forced split-K refuses M > 64; a forced 1-SM tile computes as usual.
+    M, N, K = 128, 256, 256
+    a, b, ab, bb = parity.inputs(M, N, K, "TN", "bf16", ("normal", 1.0), 93)
+    A, B = a.cuda(), b.cuda()
+    C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    monkeypatch.setenv("HGEMM_FORCE_VARIANT", "splitk")
+    with hgemm.Handle() as h:
+        assert h.run(A, B, C, layout="TN", acc="f32", check=False) == hgemm.HGEMM_ERR_UNSUPPORTED
+    monkeypatch.setenv("HGEMM_FORCE_VARIANT", "1sm128")
+    with hgemm.Handle() as h:
+        h.run(A, B, C, layout="TN", acc="f32")
+        assert h.sync_status()[0] == hgemm.HGEMM_OK
+    parity.check(workloads.bits(C.cpu()), ab, bb, M, N, K, "TN", "bf16", "f32", "bf16")
+    monkeypatch.delenv("HGEMM_FORCE_VARIANT")
+    with hgemm.Handle() as h:  # unset: automatic again
+        assert h.run(A, B, C, layout="TN", acc="f32", check=False) == hgemm.HGEMM_OK
