@@ -629,8 +629,10 @@ hgemm_status_t hgemm_run(hgemm_handle_t h, const void* A, const void* B, void* C
     if (!encode_2d(&tmW, in_dtype, B, (uint64_t)K, (uint64_t)N, 64, 128) ||
         !encode_2d(&tmX, in_dtype, A, (uint64_t)K, (uint64_t)M, 64, (uint32_t)mma_n))
       return HGEMM_ERR_CUDA;
-    const size_t partial_bytes = (size_t)p.splitk_chunks * 2 * 128 * (size_t)mma_n * sizeof(float);
-    st = ensure_workspace(h, partial_bytes, (size_t)p.num_tiles * kSplitKTicketStride, s);  // one counter per tile
+    // Whole tiles need neither partials nor counters: no tile has a second contributor.
+    const bool whole = p.splitk_align > 1;
+    const size_t partial_bytes = whole ? 0 : (size_t)p.splitk_chunks * 2 * 128 * (size_t)mma_n * sizeof(float);
+    st = ensure_workspace(h, partial_bytes, whole ? 0 : (size_t)p.num_tiles * kSplitKTicketStride, s);
     if (st != HGEMM_OK) return st;
     if ((st = inject_ticket_fault(h, s)) != HGEMM_OK) return st;
     if (p.smem_bytes > h->splitk_prepared_smem) return HGEMM_ERR_UNSUPPORTED;

@@ -52,18 +52,33 @@ def test_graph_capture_and_replay():
 
 @pytest.mark.filterwarnings("ignore:The CUDA Graph is empty")
 def test_capture_refuses_to_allocate():
-    # A fresh handle has no workspace: inside a capture the split-K launch must
-    # refuse (UNSUPPORTED, nothing enqueued) instead of calling cudaMalloc.
+    # A fresh handle has no workspace: inside a capture a split-K launch that
+    # needs one (the K split, forced here) must refuse (UNSUPPORTED, nothing
+    # enqueued) instead of calling cudaMalloc.
     M, N, K = 16, 16384, 4096
-    A, B, _, _ = _inputs(M, N, K, 131)
+    A, B, ab, bb = _inputs(M, N, K, 131)
     C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
     with hgemm.Handle() as h:
+        h.set_option(hgemm.HGEMM_OPT_STREAM_K, 2)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             st = h.run(A, B, C, check=False)
         assert st == hgemm.HGEMM_ERR_UNSUPPORTED
         assert h.run(A, B, C, check=False) == hgemm.HGEMM_OK  # outside a capture it allocates and runs
         assert h.sync_status()[0] == hgemm.HGEMM_OK
+    # Whole tiles (the planner's layout here) use no workspace: a fresh
+    # handle's launch can be captured directly.
+    with hgemm.Handle() as h:
+        st, p = hgemm.hgemm_plan(M, N, K, num_sms=torch.cuda.get_device_properties(0).multi_processor_count)
+        assert p.splitk_align == p.k_blocks and p.workspace_bytes == 0
+        C.fill_(0)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            assert h.run(A, B, C, check=False) == hgemm.HGEMM_OK
+        g.replay()
+        torch.cuda.synchronize()
+        assert h.sync_status()[0] == hgemm.HGEMM_OK
+    parity.check(workloads.bits(C.cpu()), ab, bb, M, N, K, "TN", "bf16", "f32", "bf16")
 
 
 def test_handles_on_concurrent_streams():
