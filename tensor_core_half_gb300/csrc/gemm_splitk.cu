@@ -4,16 +4,18 @@
 // (N x K values) from HBM once.  The pages contain no skinny kernel; this one
 // reuses the tcgen05 machinery of "tcgen05 for dummies: a B200 GEMM from
 // scratch" (translated) -- TMA + mbarrier ring, warp specialisation, tensor-
-// memory accumulators, persistent CTAs -- with three changes:
+// memory accumulators, persistent CTAs -- with these changes:
 //   - swap A and B: the MMA computes C^T[N,M] = B[N,K] . A[M,K]^T, so that the
 //     large N fills the MMA's 128 rows and M (padded to 16..64) is the MMA's N;
-//   - balanced split-K: the tile-major list of (128-row N tile, 64-wide K
-//     block) units is cut into one contiguous range per CTA, so every SM
-//     streams the same number of bytes of B;
-//   - deterministic reduction: a tile covered by several CTAs gets one fp32
-//     partial per CTA in a workspace; the last CTA to finish the tile (an
-//     atomic ticket) adds the partials in K order and writes C.  No float
-//     atomics, so repeated runs give identical bits.
+//   - the work is the tile-major list of (128-row N tile, 128-wide K block)
+//     units, cut into contiguous chunks (splitk_shape): whole tiles per CTA
+//     where that streams as fast, else one equal range per SM so that every
+//     SM streams the same number of bytes of B;
+//   - deterministic reduction of a tile whose K range is split: one fp32
+//     partial per contributor in a workspace; the last contributor (an
+//     atomic ticket, or all the others seen published while it computed)
+//     adds the partials in K order and writes C.  No float atomics, so
+//     repeated runs give identical bits.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
