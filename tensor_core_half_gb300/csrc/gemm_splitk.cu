@@ -101,12 +101,20 @@ namespace {
 // GB300 streaming rates behind the layout choice (a CTA streaming B tiles
 // along K through an 11-stage ring, measured with 32-152 CTAs): one CTA
 // reaches 62-68 GB/s, and the GPU as a whole about 6250 GB/s, which about 100
-// CTAs already reach.  A split of some tile's K range between CTAs costs the
-// fix-up at the end of the kernel: about 4 us measured on 16 x 16384 x 8192
-// (the same launches with the fix-ups left out).
+// CTAs already reach.  Whole tiles keep ~94 % of that in the kernel (one
+// tile per CTA, so the slowest SM ends the launch: 128 CTAs measured 5.75
+// TB/s where the balanced split streams 6.2).  A split of some tile's K
+// range between CTAs costs the fix-up at the end of the kernel: ~4 us at
+// M <= 16 (16 x 16384 x 8192, the same launches with the fix-ups left out),
+// growing with the fp32 partials, ~1.5 us per further 16 columns of M.
+// Measured choices this reproduces: whole tiles at 16 x 16384 x 8192,
+// 16 x 12288 x 8192, 32 x 14336 x 4096 and 64 x 16384 x 8192; the split at
+// 16 x 20480 x 8192, 16 x 8192 x 8192 and 1 x 16384 x 16384.
 constexpr double kSplitKCtaGBs = 62.0;
 constexpr double kSplitKGpuGBs = 6250.0;
+constexpr double kSplitKWholeEff = 0.94;
 constexpr double kSplitKFixupNs = 4000.0;
+constexpr double kSplitKFixupPer16Ns = 1500.0;
 constexpr int kSplitKSplitStages = 5;  // 180 KB in flight at M <= 16
 constexpr int kSplitKWholeStages = 6;  // 216 KB: fewer CTAs, each streaming faster
 
@@ -136,9 +144,10 @@ SplitKShape splitk_shape(int64_t tiles, int32_t k_blocks, int64_t K, int mma_n, 
       const double tile_bytes = (double)kRowsPerTile * (double)K * 2.0;
       const int64_t per = (tiles + sms - 1) / sms;
       const int64_t p_whole = (tiles + per - 1) / per;
-      const double t_whole = (double)per * tile_bytes / (splitk_rate(p_whole) / (double)p_whole);
+      const double t_whole = (double)per * tile_bytes / (kSplitKWholeEff * splitk_rate(p_whole) / (double)p_whole);
       const int64_t p_split = units < sms ? units : sms;
-      const double t_split = (double)tiles * tile_bytes / splitk_rate(p_split) + kSplitKFixupNs;
+      const double fixup = kSplitKFixupNs + kSplitKFixupPer16Ns * (double)(mma_n / 16 - 1);
+      const double t_split = (double)tiles * tile_bytes / splitk_rate(p_split) + fixup;
       whole = t_whole <= t_split;
     }
   }

@@ -158,7 +158,10 @@ def test_splitk_partition(M, N, K, sms):
     (16, 8192, 8192, 152, False, 152),    # 64 CTAs would reach ~4 TB/s: split over every SM
     (16, 20480, 8192, 152, False, 152),   # 160 tiles -> 80 CTAs of two tiles: too few
     (16, 4096, 4096, 152, False, 152),
-    (16, 16384, 8192, 148, True, 128)])
+    (16, 16384, 8192, 148, True, 128),
+    (64, 16384, 8192, 152, True, 128),    # the split's fix-up grows with M
+    (32, 14336, 4096, 152, True, 112),
+    (1, 16384, 16384, 152, False, 152)])  # long K: the slowest SM's share of a whole tile outweighs the fix-up
 def test_splitk_whole_tile_choice(M, N, K, sms, whole, grid):
     """The planner's layout for skinny products: whole tiles per CTA (no
     tile's K range split, no fix-up) when 128-row tiles at the CTA count that
