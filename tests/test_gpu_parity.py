@@ -119,6 +119,80 @@ def test_small_integers_bit_exact_f16_acc(h, variant):
     assert np.array_equal(got, ref)
 
 
+def _overflow_operands(M, N, K, layout):
+    # C[i, j] = s_j * (A[i, 0] + A[i, 1]) with s_j = +1 for even j, -1 for odd:
+    # A[i, 0] runs over fp16's largest values, A[i, 1] over small integers, so
+    # the sums cross fp16's overflow threshold (halfway between 65504 and 2^16:
+    # 65519 rounds to 65504, 65520 to infinity) on both signs.  Every partial
+    # sum is an integer below 2^24, exact in fp32 in any order.
+    big = np.array([65504.0, 65472.0, 65440.0, 32768.0], np.float32)
+    a = torch.zeros((M, K), dtype=torch.float32)
+    a[:, 0] = torch.from_numpy(big[np.arange(M) % big.size])
+    a[:, 1] = torch.from_numpy(((np.arange(M) * 7) % 81 - 40).astype(np.float32))
+    sign = torch.from_numpy(np.where(np.arange(N) % 2 == 0, 1.0, -1.0).astype(np.float32))
+    bt = torch.zeros((N, K), dtype=torch.float32)  # [N, K]
+    bt[:, 0] = sign
+    bt[:, 1] = sign
+    b = bt if layout == "TN" else bt.t().contiguous()
+    a, b = a.half(), b.half()
+    return a, b, workloads.bits(a), workloads.bits(b)
+
+
+@pytest.mark.parametrize("epilogue", ["tma", "direct"])
+@pytest.mark.parametrize("layout", ["TN", "NN"])
+@pytest.mark.parametrize("variant,M", [("auto", 300)] + [(v, 300) for v in DENSE_VARIANTS] + [("splitk", 48)])
+def test_output_overflow_rounds_like_the_oracle(h, variant, M, layout, epilogue):
+    # Rounding to fp16 output at its overflow threshold: bit-exact against the
+    # oracle's round-to-nearest-even, infinities included.
+    if variant == "splitk" and layout == "NN":
+        pytest.skip("split-K takes the TN layout")
+    if variant == "splitk" and epilogue == "direct":
+        pytest.skip("the epilogue option applies to the dense kernels")
+    N, K = 520, 64
+    a, b, ab, bb = _overflow_operands(M, N, K, layout)
+    got = run(h, a, b, M, N, K, layout, "f32", "f16", variant, epilogue=epilogue)
+    ref, _, _ = oracle.gemm(ab, bb, M, N, K, layout, "f16", "f16")
+    assert np.isinf(oracle.decode(ref.ravel(), "f16")).sum() > 0  # the threshold is crossed
+    assert np.array_equal(got, ref)
+
+
+def _nonfinite_operands(M, N, K, seed):
+    # Normal data with a +inf in row 7 of A (k = 13), whose B entries are 0, +1
+    # and -1 by column (inf * 0 = NaN, +-inf otherwise), a NaN in row M-2 of A
+    # and a -inf in column 400 of B (k = 77), which meets the +inf of row 7.
+    a, bt, _, _ = parity.inputs(M, N, K, "TN", "bf16", ("normal", 1.0), seed)
+    a, bt = a.float(), bt.float()
+    a[7, 13] = float("inf")
+    bt[:, 13] = torch.from_numpy(np.array([0.0, 1.0, -1.0], np.float32)[np.arange(N) % 3])
+    a[M - 2, 50] = float("nan")
+    bt[400, 77] = float("-inf")
+    a, bt = a.bfloat16(), bt.bfloat16()
+    return a, bt, workloads.bits(a), workloads.bits(bt)
+
+
+@pytest.mark.parametrize("variant,M,stream_k", [("auto", 300, 1), ("2sm256", 300, 2), ("1sm128", 300, 1),
+                                                ("splitk", 48, 0), ("splitk", 48, 2)])
+def test_nonfinite_inputs_propagate_like_the_oracle(h, variant, M, stream_k):
+    # Inputs are unspecified beyond finite values, but IEEE arithmetic fixes
+    # where infinities and NaNs land: NaN and inf positions and signs must be
+    # those of the oracle's double-precision sum; every finite entry is still
+    # within tolerance.  Split tiles (stream-K, the K split) add partials that
+    # hold infinities.
+    N, K = 520, 200
+    a, b, ab, bb = _nonfinite_operands(M, N, K, 23)
+    got = oracle.decode(run(h, a, b, M, N, K, "TN", "f32", "bf16", variant, stream_k=stream_k).ravel(), "bf16")
+    ref_bits, ref, absdot = oracle.gemm(ab, bb, M, N, K, "TN", "bf16", "bf16", want_exact=True, want_abs=True)
+    ref_out = oracle.decode(ref_bits.ravel(), "bf16")
+    assert np.array_equal(np.isnan(got), np.isnan(ref_out))
+    assert np.isnan(ref_out).sum() >= N and np.isinf(ref_out).sum() > 0
+    inf = np.isinf(ref_out)
+    assert np.array_equal(got[inf], ref_out[inf])
+    fin = np.isfinite(ref_out)
+    assert np.array_equal(np.isfinite(got), fin)
+    ref, absdot = ref.ravel()[fin], absdot.ravel()[fin]
+    assert (np.abs(got[fin] - ref) <= parity.bound(ref, absdot, "f32", "bf16")).all()
+
+
 @pytest.mark.parametrize("M", [1, 5, 16, 17, 33, 48, 64])
 @pytest.mark.parametrize("N,K", [(8, 64), (1000, 72), (4096, 1024), (384, 8192)])
 def test_splitk_shapes(h, M, N, K):
