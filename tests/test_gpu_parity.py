@@ -535,14 +535,37 @@ def test_run_host_back_to_back_calls(h):
     # device; every output must still be the product of its own inputs.
     M, N, K = 1536, 1024, 512
     sets = [parity.inputs(M, N, K, "TN", "f16", ("uniform", -1.0, 1.0), 90 + i) for i in range(4)]
+    # The pinned copies stay referenced until the copies have run: the host
+    # allocator may hand a freed block to the next pin_memory() at once.
+    pinned = [(a.pin_memory(), b.pin_memory()) for a, b, _, _ in sets]
     outs = []
-    for a, b, _, _ in sets:
+    for ap, bp in pinned:
         C = torch.empty((M, N), dtype=torch.float16).pin_memory()
-        h.run_host(a.pin_memory(), b.pin_memory(), C, layout="TN", acc="f32")
+        h.run_host(ap, bp, C, layout="TN", acc="f32")
         outs.append(C)
     assert h.sync_status()[0] == hgemm.HGEMM_OK
     for (a, b, ab, bb), C in zip(sets, outs):
         parity.check(workloads.bits(C), ab, bb, M, N, K, "TN", "f16", "f32", "f16")
+
+
+def test_run_host_alternating_streams(h):
+    # The benchmark's end-to-end loop: consecutive calls alternate between two
+    # caller streams, so one call's uploads overlap the previous call's GEMM
+    # and download.  Six calls reuse each staging set three times; every output
+    # must be the product of its own inputs.
+    M, N, K = 2048, 1536, 1024
+    sets = [parity.inputs(M, N, K, "TN", "bf16", ("normal", 1.0), 95 + i) for i in range(6)]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    pinned = [(a.pin_memory(), b.pin_memory()) for a, b, _, _ in sets]
+    outs = []
+    for i, (ap, bp) in enumerate(pinned):
+        C = torch.full((M, N), float("nan"), dtype=torch.bfloat16).pin_memory()
+        h.run_host(ap, bp, C, layout="TN", acc="f32", stream=streams[i % 2])
+        outs.append(C)
+    torch.cuda.synchronize()
+    assert h.sync_status()[0] == hgemm.HGEMM_OK
+    for (a, b, ab, bb), C in zip(sets, outs):
+        parity.check(workloads.bits(C), ab, bb, M, N, K, "TN", "bf16", "f32", "bf16")
 
 
 def test_env_force_variant(monkeypatch):
