@@ -62,6 +62,8 @@ WORKLOADS = {w.name: w for w in [
     Workload("square4096_bf16", 4096, 4096, 4096, "TN", "bf16", "f32", "bf16", ("normal", 1.0), 1,
              note="headline: 4096^3 bf16, fp32 accumulate"),
     *[_sweep(s, acc) for s in (2048, 4096, 8192, 12288, 16384) for acc in ("f32", "f16")],
+    Workload("square8192_bf16", 8192, 8192, 8192, "TN", "bf16", "f32", "bf16", ("normal", 1.0), 1,
+             note="8192^3 in bf16 with the headline's distribution"),
     Workload("nn8192x8192x16384_f16", 8192, 8192, 16384, "NN", "f16", "f32", "f16",
              ("uniform", -0.5, 0.5), 3, note="all row-major, B not pre-transposed"),
     Workload("ragged1000x3000x4104_bf16", 1000, 3000, 4104, "TN", "bf16", "f32", "bf16",

@@ -71,7 +71,3 @@ def test_workload_dynamic_schedule(h, name):
 def test_headline_other_variants(h, variant):
     _check(h, workloads.WORKLOADS["square4096_bf16"], variant)
 
-
-def test_bf16_8192_cubed_headline_distribution(h):
-    w = workloads.Workload("square8192_bf16", 8192, 8192, 8192, "TN", "bf16", "f32", "bf16", ("normal", 1.0), 1)
-    _check(h, w)
