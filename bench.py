@@ -28,6 +28,7 @@ Prints one JSON line (rank 0).
 from __future__ import annotations
 
 import argparse
+import atexit
 import hashlib
 import json
 import math
@@ -113,6 +114,8 @@ class ClockSampler:
         except (OSError, FileNotFoundError):
             self.proc = None
             return
+        # A run that raises before stop() must not leave nvidia-smi looping.
+        atexit.register(self.stop)
         self.thread = threading.Thread(target=self._reader, daemon=True)
         self.thread.start()
 
@@ -131,12 +134,14 @@ class ClockSampler:
             self.samples.append((time.time(), sm, mx, pw, act))
 
     def stop(self):
-        if self.proc is not None:
+        """Ends the sampling process; safe to call more than once."""
+        if self.proc is not None and self.proc.poll() is None:
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
+                self.proc.wait(timeout=5)
 
     def summary(self, t0: float, t1: float):
         inside = [s for s in self.samples if t0 <= s[0] <= t1]
