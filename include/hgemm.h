@@ -206,14 +206,17 @@ hgemm_status_t hgemm_run(hgemm_handle_t h, const void* A, const void* B, void* C
  *   Same arguments, layouts and rules as hgemm_run, except that A, B and C are
  *   host pointers (page-locked memory lets the copies run asynchronously and
  *   overlap; pageable memory works but its copies block the host).
- * B is copied to the device once; A and C move in row chunks (512 rows or
- * more, at most 8 chunks) on two internal copy streams, so that the upload of
- * chunk i+1, the GEMM of chunk i and the download of chunk i-1 overlap.  The
- * handle owns two sets of device staging buffers (allocated on first use,
- * grown on demand) and alternates between them, so consecutive calls overlap
- * too.  The work starts after earlier work on `stream`, and `stream` waits for
- * its end: C is complete once `stream` is synchronised.  A, B and C must stay
- * valid and unmodified until then.  C must not overlap A or B.
+ * B is copied to the device once; A and C move in row chunks (1024 rows or
+ * more, whole 256-row tiles, at most 4 chunks) on two internal copy streams,
+ * so that the upload of chunk i+1, the GEMM of chunk i and the download of
+ * chunk i-1 overlap.  The handle owns two sets of device staging buffers
+ * (allocated on first use, grown on demand) and alternates between them, so
+ * consecutive calls on DIFFERENT streams overlap too: one call's uploads run
+ * beside the previous call's GEMM and download.  Calls on one stream run one
+ * after another.  The work starts after earlier work on `stream`, and
+ * `stream` waits for its end: C is complete once `stream` is synchronised.
+ * A, B and C must stay valid and unmodified until then.  C must not overlap
+ * A or B.
  */
 hgemm_status_t hgemm_run_host(hgemm_handle_t h, const void* A, const void* B, void* C, int64_t M, int64_t N,
                               int64_t K, hgemm_layout_t layout, hgemm_dtype_t in_dtype, hgemm_dtype_t acc_dtype,
