@@ -568,6 +568,29 @@ def test_run_host_alternating_streams(h):
         parity.check(workloads.bits(C), ab, bb, M, N, K, "TN", "bf16", "f32", "bf16")
 
 
+def test_tensor_maps_follow_shape_and_type(h):
+    # One allocation per operand, reused with other shapes, element types and
+    # kernels (dense and split-K), then with the first again: every result
+    # must be the product of its own operands.
+    buf_a = torch.empty(1 << 20, dtype=torch.int16, device="cuda")
+    buf_b = torch.empty(1 << 21, dtype=torch.int16, device="cuda")
+    buf_c = torch.empty(1 << 20, dtype=torch.int16, device="cuda")
+    cases = [(512, 768, 1024, "bf16"), (768, 512, 1024, "bf16"), (512, 768, 512, "f16"), (16, 2048, 1024, "bf16"),
+             (16, 1024, 2048, "bf16"), (512, 768, 1024, "bf16")]
+    for i, (M, N, K, dt) in enumerate(cases):
+        a, b, ab, bb = parity.inputs(M, N, K, "TN", dt, ("normal", 1.0), 140 + i)
+        A = buf_a[:M * K].view(TORCH_DT[dt]).view(M, K)
+        B = buf_b[:N * K].view(TORCH_DT[dt]).view(N, K)
+        C = buf_c[:M * N].view(TORCH_DT[dt]).view(M, N)
+        A.copy_(a.cuda())
+        B.copy_(b.cuda())
+        C.fill_(float("nan"))
+        h.run(A, B, C, layout="TN", acc="f32")
+        st, detail = h.sync_status()
+        assert st == hgemm.HGEMM_OK, hex(detail)
+        parity.check(workloads.bits(C.cpu()), ab, bb, M, N, K, "TN", dt, "f32", dt)
+
+
 def test_env_force_variant(monkeypatch):
     # HGEMM_FORCE_VARIANT pins the variant of the handles created while it is
     # set: forced split-K refuses M > 64; a forced 1-SM tile computes as usual.
