@@ -1,0 +1,96 @@
+"""bench.py's measurement plumbing on the CPU: nvidia-smi parsing, the clock
+summary of the timed window, and when stored ncu traffic may be reported."""
+import io
+import json
+import math
+import os
+from types import SimpleNamespace
+
+import bench
+
+
+def _sampler(samples=None, lines=None):
+    s = bench.ClockSampler.__new__(bench.ClockSampler)  # no nvidia-smi process
+    s.samples = list(samples or [])
+    s.thread = None
+    s.proc = SimpleNamespace(stdout=io.StringIO(lines or ""), poll=lambda: 0)
+    return s
+
+
+def test_reader_parses_hex_and_decimal_masks_and_skips_junk():
+    lines = ("0, 2070, 2070, 441.50, 0x0000000000000004, Not Active, Not Active, Not Active, Active\n"
+             "0, 1980, 2070, [N/A], 12, Active, Not Active, Not Active, Active\n"
+             "garbage line\n"
+             "0, notanumber, 2070, 400, 0x0\n")
+    s = _sampler(lines=lines)
+    s._reader()
+    assert len(s.samples) == 2
+    _, sm, mx, pw, act = s.samples[0]
+    assert (sm, mx, pw, act) == (2070.0, 2070.0, 441.5, 0x4)
+    _, sm, mx, pw, act = s.samples[1]
+    assert (sm, mx, act) == (1980.0, 2070.0, 12) and math.isnan(pw)
+
+
+def test_summary_keeps_the_timed_window_and_names_the_reasons():
+    samples = [(0.5, 1000.0, 2070.0, 100.0, 0x8),     # before the window: ignored
+               (1.0, 2070.0, 2070.0, 900.0, 0x4),
+               (1.5, 2000.0, 2070.0, float("nan"), 0x0),
+               (2.0, 2065.0, 2070.0, 1200.0, 0x4),
+               (3.5, 500.0, 2070.0, 50.0, 0x40)]      # after: ignored
+    out = _sampler(samples).summary(1.0, 2.0)
+    assert out["window"] == "timed" and out["samples"] == 3
+    assert out["sm_mhz"] == 2065.0 and out["sm_max_mhz"] == 2070.0
+    assert out["reasons"] == ["sw_power_cap"]
+    assert out["power_w_max"] == 1200.0
+
+
+def test_summary_reports_slowdowns_seen_inside_the_window():
+    samples = [(1.0, 1500.0, 2070.0, 1000.0, 0x8 | 0x20), (1.1, 1600.0, 2070.0, 1000.0, 0x40)]
+    out = _sampler(samples).summary(0.9, 1.2)
+    assert set(out["reasons"]) == {"hw_slowdown", "sw_thermal_slowdown", "hw_thermal_slowdown"}
+
+
+def test_summary_falls_back_to_the_nearest_samples_or_none():
+    samples = [(0.0, 2000.0, 2070.0, 10.0, 0), (10.0, 2010.0, 2070.0, 10.0, 0), (20.0, 2020.0, 2070.0, 10.0, 0),
+               (30.0, 2030.0, 2070.0, 10.0, 0)]
+    out = _sampler(samples).summary(10.4, 10.5)  # shorter than the sampling period
+    assert out["window"] == "nearest" and out["samples"] == 3
+    empty = _sampler([]).summary(0.0, 1.0)
+    assert empty["window"] == "none" and empty["sm_mhz"] is None and empty["samples"] == 0
+
+
+def test_stop_is_safe_without_a_process():
+    s = _sampler()
+    s.proc = None
+    s.stop()
+    s.stop()
+
+
+def _stored():
+    with open(os.path.join(bench.ROOT, "profiles", "traffic.json")) as f:
+        return {k: v for k, v in json.load(f).items() if not k.startswith("_")}
+
+
+def test_traffic_is_reported_only_for_the_captured_kernel_and_plan():
+    stored = _stored()
+    assert stored, "the committed ncu summaries record traffic"
+    for key, e in stored.items():
+        workload, variant = key.rsplit("/", 1)
+        kernel = "splitk" if int(variant) == 4 else "dense"
+        plan = SimpleNamespace(**e["plan"])
+        got = bench.load_traffic(workload, int(variant), plan)
+        if e["kernel_hash"] == bench.kernel_source_hash(kernel):
+            assert got == e["dram_bytes_per_launch"]
+        else:
+            assert got is None  # the kernel changed since the capture
+        other = SimpleNamespace(**dict(e["plan"], grid=e["plan"]["grid"] + 2))
+        assert bench.load_traffic(workload, int(variant), other) is None  # another launch plan
+    assert bench.load_traffic("no_such_workload", 3, None) is None
+
+
+def test_kernel_hash_covers_every_source_it_names():
+    for kernel, files in bench.KERNEL_SOURCES.items():
+        for rel in files:
+            assert os.path.exists(os.path.join(bench.ROOT, "tensor_core_half_gb300", "csrc", rel)), rel
+        h = bench.kernel_source_hash(kernel)
+        assert len(h) == 16 and h == bench.kernel_source_hash(kernel)
