@@ -44,31 +44,36 @@ def build(force: bool = False) -> str:
     return _LIB
 
 
+def _bind(path: str):
+    """The library at `path` with its entry points' argument types declared."""
+    lib = ctypes.CDLL(path)
+    u16p = ctypes.POINTER(ctypes.c_uint16)
+    f64p = ctypes.POINTER(ctypes.c_double)
+    i64p = ctypes.POINTER(ctypes.c_int64)
+    i64 = ctypes.c_int64
+    lib.oracle_decode.restype = ctypes.c_double
+    lib.oracle_decode.argtypes = [ctypes.c_uint16, ctypes.c_int]
+    lib.oracle_encode.restype = ctypes.c_uint16
+    lib.oracle_encode.argtypes = [ctypes.c_double, ctypes.c_int]
+    lib.oracle_decode_array.argtypes = [u16p, f64p, i64, ctypes.c_int]
+    lib.oracle_encode_array.argtypes = [f64p, u16p, i64, ctypes.c_int]
+    lib.oracle_gemm.restype = ctypes.c_int
+    lib.oracle_gemm.argtypes = [u16p, u16p, i64, i64, i64, ctypes.c_int, ctypes.c_int,
+                                ctypes.c_int, u16p, f64p, f64p, ctypes.c_int]
+    lib.oracle_gemm_entries.restype = ctypes.c_int
+    lib.oracle_gemm_entries.argtypes = [u16p, u16p, i64, i64, i64, ctypes.c_int, ctypes.c_int,
+                                        i64p, i64p, i64, f64p, f64p, ctypes.c_int]
+    lib.oracle_gemm_tiled.restype = ctypes.c_int
+    lib.oracle_gemm_tiled.argtypes = [u16p, u16p, i64, i64, i64, ctypes.c_int, ctypes.c_int,
+                                      i64, i64, i64, f64p]
+    return lib
+
+
 def _load():
     global _lib
     with _lock:
         if _lib is None:
-            lib = ctypes.CDLL(build())
-            u16p = ctypes.POINTER(ctypes.c_uint16)
-            f64p = ctypes.POINTER(ctypes.c_double)
-            i64p = ctypes.POINTER(ctypes.c_int64)
-            i64 = ctypes.c_int64
-            lib.oracle_decode.restype = ctypes.c_double
-            lib.oracle_decode.argtypes = [ctypes.c_uint16, ctypes.c_int]
-            lib.oracle_encode.restype = ctypes.c_uint16
-            lib.oracle_encode.argtypes = [ctypes.c_double, ctypes.c_int]
-            lib.oracle_decode_array.argtypes = [u16p, f64p, i64, ctypes.c_int]
-            lib.oracle_encode_array.argtypes = [f64p, u16p, i64, ctypes.c_int]
-            lib.oracle_gemm.restype = ctypes.c_int
-            lib.oracle_gemm.argtypes = [u16p, u16p, i64, i64, i64, ctypes.c_int, ctypes.c_int,
-                                        ctypes.c_int, u16p, f64p, f64p, ctypes.c_int]
-            lib.oracle_gemm_entries.restype = ctypes.c_int
-            lib.oracle_gemm_entries.argtypes = [u16p, u16p, i64, i64, i64, ctypes.c_int, ctypes.c_int,
-                                                i64p, i64p, i64, f64p, f64p, ctypes.c_int]
-            lib.oracle_gemm_tiled.restype = ctypes.c_int
-            lib.oracle_gemm_tiled.argtypes = [u16p, u16p, i64, i64, i64, ctypes.c_int, ctypes.c_int,
-                                              i64, i64, i64, f64p]
-            _lib = lib
+            _lib = _bind(build())
     return _lib
 
 
