@@ -369,8 +369,7 @@ class Handle:
     def run(self, A, B, C, layout="TN", acc="f32", stream=None, check=True):
         """C = A . B on torch CUDA tensors (A [M,K]; B [N,K] for TN or [K,N] for NN; C [M,N])."""
         import torch
-        M, K = A.shape
-        N = B.shape[0] if layout == "TN" else B.shape[1]
+        M, N, K = operand_shape(A, B, C, layout, cuda=True)
         s = stream if stream is not None else torch.cuda.current_stream()
         st = hgemm_run(self.h, A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, LAYOUTS[layout],
                        _torch_dtype(A.dtype), DTYPES[acc], _torch_dtype(C.dtype), s.cuda_stream)
@@ -379,11 +378,37 @@ class Handle:
         return st
 
 
+def operand_shape(A, B, C, layout, cuda):
+    """(M, N, K) of C = A . B after checking that the three tensors describe one
+    product the C ABI can take: 2-D, packed row-major (contiguous), on the right
+    side (CUDA tensors for hgemm_run, host tensors for hgemm_run_host), A and B
+    of one element type, B [N,K] (TN) or [K,N] (NN) with A's K, C [M,N].  The
+    library receives bare pointers and sizes, so a view that breaks any of these
+    would otherwise be read as something else; ValueError names the mismatch."""
+    if layout not in LAYOUTS:
+        raise ValueError("layout must be one of %s" % sorted(LAYOUTS))
+    for name, t in (("A", A), ("B", B), ("C", C)):
+        if t.dim() != 2:
+            raise ValueError("%s must be 2-D, got shape %s" % (name, tuple(t.shape)))
+        if not t.is_contiguous():
+            raise ValueError("%s must be contiguous (packed row-major)" % name)
+        if bool(t.is_cuda) != cuda:
+            raise ValueError("%s must be a %s tensor" % (name, "CUDA" if cuda else "host (CPU)"))
+    if A.dtype != B.dtype:
+        raise ValueError("A and B must share one element type, got %s and %s" % (A.dtype, B.dtype))
+    M, K = A.shape
+    N, Kb = (B.shape[0], B.shape[1]) if layout == "TN" else (B.shape[1], B.shape[0])
+    if Kb != K:
+        raise ValueError("B holds K = %d for layout %s, A holds K = %d" % (Kb, layout, K))
+    if tuple(C.shape) != (M, N):
+        raise ValueError("C must be [%d, %d], got %s" % (M, N, tuple(C.shape)))
+    return int(M), int(N), int(K)
+
+
 def _run_host_method(self, A, B, C, layout="TN", acc="f32", stream=None, check=True):
     """C = A . B on CPU tensors (pinned for overlap); returns once enqueued."""
     import torch
-    M, K = A.shape
-    N = B.shape[0] if layout == "TN" else B.shape[1]
+    M, N, K = operand_shape(A, B, C, layout, cuda=False)
     s = stream if stream is not None else torch.cuda.current_stream()
     st = hgemm_run_host(self.h, A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, LAYOUTS[layout],
                         _torch_dtype(A.dtype), DTYPES[acc], _torch_dtype(C.dtype), s.cuda_stream)

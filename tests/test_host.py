@@ -452,3 +452,28 @@ def test_trace_summary_and_chrome_format():
     doc = trace.chrome_trace(rows)
     names = sorted(e["name"] for e in doc["traceEvents"])
     assert names.count("tile 5") == 3 and "kernel_end" in names
+
+
+def test_operand_shape_accepts_one_product_and_names_each_mismatch():
+    f16, bf16 = torch.float16, torch.bfloat16
+    A = torch.zeros((6, 16), dtype=f16)
+    B_tn = torch.zeros((8, 16), dtype=f16)
+    B_nn = torch.zeros((16, 8), dtype=f16)
+    C = torch.zeros((6, 8), dtype=f16)
+    assert H.operand_shape(A, B_tn, C, "TN", cuda=False) == (6, 8, 16)
+    assert H.operand_shape(A, B_nn, C, "NN", cuda=False) == (6, 8, 16)
+    assert H.operand_shape(A[:, :0].contiguous(), B_tn[:, :0].contiguous(), C, "TN", cuda=False) == (6, 8, 0)
+    bad = [
+        ((A, B_tn, C, "TT"), "layout"),
+        ((A, B_nn.t(), C, "TN"), "contiguous"),           # a transposed view is not packed
+        ((A, B_tn, C.t().contiguous().t(), "TN"), "contiguous"),
+        ((A, B_tn.to(bf16), C, "TN"), "element type"),
+        ((A, B_nn, C, "TN"), "K"),                         # NN storage passed as TN
+        ((A, B_tn, C[:, :4], "TN"), "C must be"),
+        ((A.unsqueeze(0), B_tn, C, "TN"), "2-D"),
+    ]
+    for args, word in bad:
+        with pytest.raises(ValueError, match=word):
+            H.operand_shape(*args, cuda=False)
+    with pytest.raises(ValueError, match="CUDA"):
+        H.operand_shape(A, B_tn, C, "TN", cuda=True)      # host tensors handed to the device call
