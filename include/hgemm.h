@@ -140,8 +140,8 @@ typedef enum { HGEMM_SCHEDULE_STATIC = 0, HGEMM_SCHEDULE_DYNAMIC = 1 } hgemm_sch
  * kind: 1 kernel begin, 2 kernel end (after setup / before teardown; value =
  * the SM cycle counter's low 31 bits, so cycles / ns gives the clock), 3 item
  * begin, 4 item end, 5 stream-K or split-K partial stored and its ticket
- * drawn (value = ticket), 6 split tile reduced (value = contributors), 7 cycles the role spent blocked on its
- * barriers during the item (value).  item = tile index (-1 if none); value
+ * drawn (value = ticket), 6 split tile reduced (value = contributors),
+ * 7 cycles the role spent blocked on its barriers during the item (value).  item = tile index (-1 if none); value
  * for item begin/end = first / last k-block (epilogue: the stream-K slot). */
 typedef struct {
   uint64_t t_ns;
@@ -185,10 +185,11 @@ hgemm_status_t hgemm_destroy(hgemm_handle_t h);
  * pitch is a multiple of 16 bytes, a TMA requirement).  K == 0 skips the K
  * check and A, B may then be null.
  * Asynchronous: returns once the kernel is enqueued.  A device-side timeout
- * is reported later by hgemm_sync_status.  Split-K and stream-K launches use a
- * workspace that the handle allocates on first use (cudaMalloc; HGEMM_ERR_OOM
- * on failure); consecutive launches on different streams must not overlap
- * when they share a handle.
+ * is reported later by hgemm_sync_status.  Stream-K launches and split-K
+ * launches that split a tile's K range use a workspace that the handle
+ * allocates on first use (cudaMalloc; HGEMM_ERR_OOM on failure); plans without
+ * stream-K and split-K plans of whole tiles need none.  Consecutive launches
+ * on different streams must not overlap when they share a handle.
  * CUDA graphs: hgemm_run may be captured into a graph.  A capture cannot
  * contain the workspace allocation, so warm the handle up outside the
  * capture with the largest problem the graph will hold; during a capture a
