@@ -385,8 +385,8 @@ uint64_t hgemm_encode_smem_desc(uint32_t smem_addr, uint32_t lbo_bytes, uint32_t
  *   A: device pointer, M x K row-major; B: device pointer, N x K row-major
  *   (TN); C: device pointer, M x N row-major, written.  The caller owns all three.
  *   Limits: 1 <= M <= 64 and N <= 33,554,432 (two counters for each of the
- *   ceil(N/128) tiles fit in 2 MiB); larger sizes return HGEMM_ERR_UNSUPPORTED.  M == 0 or N == 0 is a
- *   no-op; K == 0 writes +0.  Alignment and aliasing rules are those of
+ *   ceil(N/128) tiles fit in 2 MiB); larger sizes return
+ *   HGEMM_ERR_UNSUPPORTED.  M == 0 or N == 0 is a no-op; K == 0 writes +0.  Alignment and aliasing rules are those of
  *   hgemm_run (HGEMM_ERR_MISALIGNED, HGEMM_ERR_ALIAS, HGEMM_ERR_INVALID_ARG).
  *   in_dtype, out_dtype: HGEMM_F16 or HGEMM_BF16.
  * The first call on each device does a one-time set-up with that device
