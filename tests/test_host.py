@@ -477,3 +477,20 @@ def test_operand_shape_accepts_one_product_and_names_each_mismatch():
             H.operand_shape(*args, cuda=False)
     with pytest.raises(ValueError, match="CUDA"):
         H.operand_shape(A, B_tn, C, "TN", cuda=True)      # host tensors handed to the device call
+
+
+@pytest.mark.parametrize("M,N,K", [(4096, 4096, 4096), (2048, 2048, 2048), (1000, 3000, 4104), (16, 16384, 8192),
+                                   (16, 8192, 8192), (1, 16384, 16384), (64, 16384, 8192), (256, 256, 256)])
+@pytest.mark.parametrize("stream_k", [0, 1, 2])
+def test_workspace_only_where_a_tile_is_split(M, N, K, stream_k):
+    # A launch needs the workspace (fp32 partials and fix-up counters) exactly
+    # when some tile's K range is split: dense stream-K, or a split-K plan
+    # that is not whole tiles.  Whole-tile plans allocate nothing, which is
+    # what lets them be captured into a graph on a fresh handle.
+    st, p = H.hgemm_plan(M, N, K, num_sms=152, stream_k=stream_k)
+    assert st == ST_OK
+    if p.variant == H.HGEMM_VARIANT_SPLITK:
+        split = p.splitk_align == 1
+    else:
+        split = p.stream_k == 1
+    assert (p.workspace_bytes > 0) == split, (p.variant, p.stream_k, p.splitk_align, p.workspace_bytes)
