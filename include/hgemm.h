@@ -176,7 +176,9 @@ hgemm_status_t hgemm_destroy(hgemm_handle_t h);
  *   B: device pointer; TN: stored N x K row-major (element B[k][n] at B + n*K + k);
  *      NN: stored K x N row-major (element B[k][n] at B + k*N + n).
  *   C: device pointer, M x N, row-major, written (never read).  Must not overlap A or B.
- *   M, N, K >= 0, each <= 2^31 - 1.  M == 0 or N == 0: nothing to do, HGEMM_OK.
+ *   M, N, K >= 0, each <= 2^31 - 1, and ceil(M/128) * ceil(N/128) <= 2^31 - 1
+ *      (the tile count is 32-bit); INVALID_ARG otherwise.
+ *      M == 0 or N == 0: nothing to do, HGEMM_OK.
  *      K == 0: C is filled with +0 (the empty sum).
  *   in_dtype:  HGEMM_F16 or HGEMM_BF16 (A and B share it).
  *   acc_dtype: HGEMM_F32, or HGEMM_F16 with in_dtype == HGEMM_F16.

@@ -103,6 +103,10 @@ int env_force_variant() {
 // Checks that do not involve pointers.  Order: sizes, enums, combinations, pitches.
 hgemm_status_t check_problem(int64_t M, int64_t N, int64_t K, int layout, int in, int acc, int out) {
   if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return HGEMM_ERR_INVALID_ARG;
+  // Tile counts are 32-bit in the plans and on the device: the smallest tile
+  // (128 x 128) must leave them in range (each factor is below 2^24 here, so
+  // the product cannot overflow 64 bits).
+  if (((M + 127) / 128) * ((N + 127) / 128) > (int64_t)INT32_MAX) return HGEMM_ERR_INVALID_ARG;
   if (layout != HGEMM_LAYOUT_TN && layout != HGEMM_LAYOUT_NN) return HGEMM_ERR_INVALID_ARG;
   if (!valid_dtype(in) || !valid_dtype(acc) || !valid_dtype(out)) return HGEMM_ERR_INVALID_ARG;
   if (in == HGEMM_F32 || out == HGEMM_F32) return HGEMM_ERR_UNSUPPORTED;

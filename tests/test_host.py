@@ -494,3 +494,16 @@ def test_workspace_only_where_a_tile_is_split(M, N, K, stream_k):
     else:
         split = p.stream_k == 1
     assert (p.workspace_bytes > 0) == split, (p.variant, p.stream_k, p.splitk_align, p.workspace_bytes)
+
+
+def test_tile_count_beyond_32_bits_is_rejected():
+    # Each dimension is allowed up to 2^31 - 1, but the 128 x 128 tile count
+    # must stay 32-bit: the largest square product that fits is accepted, the
+    # next size up is refused before any plan is made.
+    big = 2 ** 31 - 8
+    st, _ = H.hgemm_plan(big, big, 64, num_sms=152)
+    assert st == H.HGEMM_ERR_INVALID_ARG
+    st, _ = H.hgemm_plan(128 * 46340, 128 * 46340, 64, num_sms=152)   # 46340^2 < 2^31 tiles
+    assert st == ST_OK
+    st, _ = H.hgemm_plan(128 * 46341, 128 * 46341, 64, num_sms=152)   # 46341^2 > 2^31 - 1
+    assert st == H.HGEMM_ERR_INVALID_ARG
