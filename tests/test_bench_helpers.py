@@ -94,3 +94,23 @@ def test_kernel_hash_covers_every_source_it_names():
             assert os.path.exists(os.path.join(bench.ROOT, "tensor_core_half_gb300", "csrc", rel)), rel
         h = bench.kernel_source_hash(kernel)
         assert len(h) == 16 and h == bench.kernel_source_hash(kernel)
+
+
+def test_reference_arm_prints_the_contract_line():
+    # The reference arm times the oracle on the host cores and prints one JSON
+    # line with the same metric and config as the CUDA arm, marked as such.
+    import subprocess
+    import sys
+    r = subprocess.run([sys.executable, os.path.join(bench.ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "3"], capture_output=True, text=True, timeout=600, cwd=bench.ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 1 and d["steps"] == 1 and d["warmup"] == 3
+    assert d["metric"].startswith("TFLOPS") and d["unit"] == "TFLOPS" and d["higher_is_better"] is True
+    assert d["value"] > 0 and d["ms_per_step"] > 0 and d["vs_baseline"] is None
+    assert d["data"] == "synthetic" and d["config"]["workload"] == "square4096_bf16"
+    cpu = d["cpu_baseline"]
+    assert cpu["kind"] == "oracle" and cpu["cores"] >= 1 and cpu["value"] == d["value"] and cpu["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
