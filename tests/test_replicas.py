@@ -34,3 +34,23 @@ def test_max_over_ranks_two_gloo_ranks():
     out = mgr.dict()
     mp.start_processes(_rank_main, args=(world, _free_port(), out), nprocs=world, start_method="spawn", join=True)
     assert dict(out) == {0: 15.0, 1: 15.0}
+
+
+@pytest.mark.timeout(300)
+def test_reference_arm_under_torchrun_prints_once():
+    # Launched the way the scaling run launches it (torchrun, two ranks): rank 0
+    # alone times the oracle and prints the line; the other rank exits 0
+    # without work.
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2", "--master-addr",
+           "127.0.0.1", "--master-port", str(_free_port()), os.path.join(root, "bench.py"), "--impl", "reference",
+           "--gpus", "2", "--steps", "1", "--warmup", "3"]
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=280, cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
