@@ -1,4 +1,7 @@
-"""The intra-kernel tracer records exactly the schedule the planner describes."""
+"""The intra-kernel tracer records exactly the schedule the planner describes,
+and a traced launch still computes the right C: tracing adds global stores to
+every role of both kernels (producer, MMA issuer, epilogue, stream-K and
+split-K fix-ups), so every traced result is checked against the oracle."""
 import collections
 
 import pytest
@@ -10,28 +13,64 @@ from tensor_core_half_gb300 import hgemm, trace
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("variant,M,N,K", [("2sm256", 1024, 1280, 1024), ("1sm128", 640, 1000, 4104),
-                                           ("splitk", 16, 4096, 4096)])
-def test_trace_matches_plan(variant, M, N, K):
+def _traced_run(h, M, N, K, seed, capacity):
+    """Runs one traced bf16 TN product, checks C against the oracle (in full:
+    every shape here is small enough) and returns the trace records."""
+    a, b, ab, bb = parity.inputs(M, N, K, "TN", "bf16", ("normal", 1.0), seed)
+    A, B = a.cuda(), b.cuda()
+    C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    h.run(A, B, C, layout="TN", acc="f32")
+    st, detail = h.sync_status()
+    assert st == hgemm.HGEMM_OK, (st, hex(detail))
+    st, n, rows = hgemm.hgemm_trace_read(h.h, capacity)
+    assert st == hgemm.HGEMM_OK and n == len(rows) > 0
+    got = C.view(torch.int16).cpu().numpy().view("uint16")
+    parity.check(got, ab, bb, M, N, K, "TN", "bf16", "f32", "bf16")
+    return rows
+
+
+# Stream-K 2 splits every tile of a partial wave between clusters, so the
+# traced fix-up path (partials published, the last contributor's reduction)
+# runs on every tile; 3 cuts the tiles left after whole waves into equal K
+# pieces; the split-K cases run the whole-tile and the balanced split layouts.
+TRACE_CASES = [("2sm256", 1024, 1280, 1024, 1), ("1sm128", 640, 1000, 4104, 1), ("splitk", 16, 4096, 4096, 1),
+               ("2sm256", 1000, 3000, 4104, 2), ("2sm192", 768, 520, 4104, 2), ("1sm256", 640, 1000, 1032, 2),
+               ("1sm128", 256, 264, 200, 2), ("splitk", 48, 3000, 2000, 2), ("splitk", 16, 16384, 2048, 0),
+               ("2sm256", 4096, 2560, 512, 3), ("1sm128", 1000, 3000, 520, 3)]
+
+
+@pytest.mark.parametrize("variant,M,N,K,sk", TRACE_CASES)
+def test_trace_matches_plan(variant, M, N, K, sk):
     with hgemm.Handle() as h:
         h.set_option(hgemm.HGEMM_OPT_FORCE_VARIANT, hgemm.VARIANTS[variant])
+        h.set_option(hgemm.HGEMM_OPT_STREAM_K, sk)
         h.set_option(hgemm.HGEMM_OPT_TRACE, 1 << 16)
-        a, b, _, _ = parity.inputs(M, N, K, "TN", "bf16", ("normal", 1.0), 71)
-        A, B = a.cuda(), b.cuda()
-        C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
-        h.run(A, B, C, layout="TN", acc="f32")
-        assert h.sync_status()[0] == hgemm.HGEMM_OK
-        st, n, rows = hgemm.hgemm_trace_read(h.h, 1 << 16)
-        assert st == hgemm.HGEMM_OK and n == len(rows) > 0
+        rows = _traced_run(h, M, N, K, 71, 1 << 16)
         st2, n2, _ = hgemm.hgemm_trace_read(h.h, 16)
         assert st2 == hgemm.HGEMM_OK and n2 == 0  # reading empties the buffer
+        # The same handle with tracing off gives the same bits: the trace
+        # records add stores but change neither the schedule nor the sums.
+        h.set_option(hgemm.HGEMM_OPT_TRACE, 0)
+        a, b, _, _ = parity.inputs(M, N, K, "TN", "bf16", ("normal", 1.0), 71)
+        A, B = a.cuda(), b.cuda()
+        C0 = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        C1 = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        h.run(A, B, C0, layout="TN", acc="f32")
+        h.set_option(hgemm.HGEMM_OPT_TRACE, 1 << 16)
+        h.run(A, B, C1, layout="TN", acc="f32")
+        assert h.sync_status()[0] == hgemm.HGEMM_OK
+        assert torch.equal(C0.view(torch.int16), C1.view(torch.int16))
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     st, p = hgemm.hgemm_plan(M, N, K, 0, hgemm.HGEMM_BF16, hgemm.HGEMM_F32, hgemm.HGEMM_BF16, sms,
-                             hgemm.VARIANTS[variant])
+                             hgemm.VARIANTS[variant], 0, sk)
     kinds = collections.Counter((r[2], r[3]) for r in rows)
     assert kinds[(0, 1)] == p.grid and kinds[(0, 2)] == p.grid  # every CTA begins and ends
     if variant == "splitk":
         return
+    if sk == 2:
+        assert p.stream_k and p.dp_tiles == 0  # every tile is split
+    if sk == 3:
+        assert p.stream_k and p.sk_pieces >= 2 and p.dp_tiles > 0  # whole waves, then equal K pieces
     clusters = p.grid // p.cta_group
     items, partials = 0, 0
     for c in range(clusters):
@@ -78,13 +117,7 @@ def test_dynamic_schedule_takes_over_pending_clusters(variant, M, N, K, sk):
         h.set_option(hgemm.HGEMM_OPT_STREAM_K, sk)
         h.set_option(hgemm.HGEMM_OPT_SCHEDULE, hgemm.HGEMM_SCHEDULE_DYNAMIC)
         h.set_option(hgemm.HGEMM_OPT_TRACE, 1 << 18)
-        a, b, _, _ = parity.inputs(M, N, K, "TN", "bf16", ("normal", 1.0), 72)
-        A, B = a.cuda(), b.cuda()
-        C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
-        h.run(A, B, C, layout="TN", acc="f32")
-        assert h.sync_status()[0] == hgemm.HGEMM_OK
-        st, n, rows = hgemm.hgemm_trace_read(h.h, 1 << 18)
-        assert st == hgemm.HGEMM_OK and n == len(rows) > 0
+        rows = _traced_run(h, M, N, K, 72, 1 << 18)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     st, p = hgemm.hgemm_plan(M, N, K, 0, hgemm.HGEMM_BF16, hgemm.HGEMM_F32, hgemm.HGEMM_BF16, sms,
                              hgemm.VARIANTS[variant], 0, sk)
@@ -117,13 +150,7 @@ def test_dynamic_splitk_takes_over_small_chunks():
     with hgemm.Handle() as h:
         h.set_option(hgemm.HGEMM_OPT_SCHEDULE, hgemm.HGEMM_SCHEDULE_DYNAMIC)
         h.set_option(hgemm.HGEMM_OPT_TRACE, 1 << 18)
-        a, b, _, _ = parity.inputs(M, N, K, "TN", "bf16", ("normal", 1.0), 73)
-        A, B = a.cuda(), b.cuda()
-        C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
-        h.run(A, B, C, layout="TN", acc="f32")
-        assert h.sync_status()[0] == hgemm.HGEMM_OK
-        st, n, rows = hgemm.hgemm_trace_read(h.h, 1 << 18)
-        assert st == hgemm.HGEMM_OK and n == len(rows) > 0
+        rows = _traced_run(h, M, N, K, 73, 1 << 18)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     st, p = hgemm.hgemm_plan(M, N, K, num_sms=sms, schedule=hgemm.HGEMM_SCHEDULE_DYNAMIC)
     assert p.variant == hgemm.HGEMM_VARIANT_SPLITK and p.splitk_chunks > p.grid
@@ -143,13 +170,7 @@ def test_splitk_segments_in_plan_order(M, N, K):
     segments in the order the planner gives (longest last)."""
     with hgemm.Handle() as h:
         h.set_option(hgemm.HGEMM_OPT_TRACE, 1 << 18)
-        a, b, _, _ = parity.inputs(M, N, K, "TN", "bf16", ("normal", 1.0), 75)
-        A, B = a.cuda(), b.cuda()
-        C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
-        h.run(A, B, C, layout="TN", acc="f32")
-        assert h.sync_status()[0] == hgemm.HGEMM_OK
-        st, n, rows = hgemm.hgemm_trace_read(h.h, 1 << 18)
-        assert st == hgemm.HGEMM_OK and n == len(rows) > 0
+        rows = _traced_run(h, M, N, K, 75, 1 << 18)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     st, p = hgemm.hgemm_plan(M, N, K, num_sms=sms)
     assert p.variant == hgemm.HGEMM_VARIANT_SPLITK
