@@ -69,8 +69,9 @@ typedef enum {
 typedef enum {
   HGEMM_OPT_FORCE_VARIANT = 1, /* value: an hgemm_variant_t; AUTO restores automatic choice   */
   HGEMM_OPT_TIMEOUT_NS = 2,    /* value: limit of every device-side wait, ns (default 2e9)    */
-  HGEMM_OPT_INJECT_FAULT = 3,  /* value: 0 off; 1 = the first CTA's producer drops its first
-                                  stage, so the consumer's bounded wait must give up; 2 = the
+  HGEMM_OPT_INJECT_FAULT = 3,  /* value: 0 off; 1 = the producers of the first CTA (both CTAs
+                                  of a pair) drop their first stage, issuing no copy for it,
+                                  so the consumer's bounded wait must give up; 2 = the
                                   host fills the fix-up ticket counters with 0x01 bytes before
                                   a stream-K or split-K launch, which HGEMM_OPT_CHECKS must
                                   report (tests)                                              */
@@ -79,7 +80,10 @@ typedef enum {
   HGEMM_OPT_STREAM_K = 6,      /* value: 1 (default) lets the planner split the last wave of
                                   dense tiles along K (stream-K) when its estimate favours it;
                                   0 keeps every tile whole; 2 splits whenever the tile count
-                                  leaves a partial wave.  Split-K (skinny M) plans likewise:
+                                  leaves a partial wave, into one equal range per cluster; 3
+                                  splits each leftover tile into equal K pieces (as many as
+                                  fit the clusters, at least 2; else as 2).  Split-K (skinny
+                                  M) plans likewise (3 acts as 2):
                                   1 chooses between whole tiles per CTA and the balanced
                                   K split over every SM by estimate, 0 always takes whole
                                   tiles, 2 always splits                                     */
@@ -87,11 +91,15 @@ typedef enum {
                                   kernels append to (0 = off, the default); hgemm_trace_read */
   HGEMM_OPT_SCHEDULE = 8,      /* value: an hgemm_schedule_t for the dense kernels           */
   HGEMM_OPT_EPILOGUE = 9,      /* value: an hgemm_epilogue_t for the dense kernels           */
-  HGEMM_OPT_CHECKS = 10        /* value: 1 = the kernels check their invariants (work ids from
+  HGEMM_OPT_CHECKS = 10,       /* value: 1 = the kernels check their invariants (work ids from
                                   launch control in range, work items and tiles in range,
                                   fix-up tickets not past the contributor count, partial
                                   slots in range) and report a violation as HGEMM_ERR_CHECK
                                   instead of trapping; 0 (default) = no checks              */
+  HGEMM_OPT_PDL_PREFETCH = 12  /* value: 0..64; dense kernels: before waiting for the
+                                  previous kernel in the stream, the producer prefetches into
+                                  L2 this many k-blocks of its first work item (0 = none,
+                                  the default)                                               */
 } hgemm_option_t;
 
 /* Check numbers reported with HGEMM_ERR_CHECK (detail bits 8-15). */
@@ -283,14 +291,18 @@ typedef struct {
                                 small chunks)                                             */
   int32_t splitk_align;  /* split-K: k_blocks when every chunk is whole tiles (no tile's K
                             range is split, no partials or fix-up), else 1                */
+  int32_t sk_pieces;     /* dense stream-K: 0 when the split k-blocks are cut into one equal
+                            range per cluster (sk_ranges = clusters); p >= 2 when each split
+                            tile is cut into p equal K pieces (sk_ranges = split tiles * p
+                            <= clusters), so that all pieces walk K side by side          */
 } hgemm_plan_t;
 
 /*
  * hgemm_plan -- the launch plan hgemm_run would use for these arguments on a
  * GPU with `num_sms` SMs (cluster capacity assumed num_sms / 2 pairs).
  * `variant` = HGEMM_VARIANT_AUTO or a forced variant; group_m = 0 for the
- * default; stream_k = 1 to allow stream-K, 0 to forbid it, 2 to force it
- * (as HGEMM_OPT_STREAM_K).  Validates the
+ * default; stream_k = 1 to allow stream-K, 0 to forbid it, 2 to force equal
+ * ranges, 3 to force equal K pieces (as HGEMM_OPT_STREAM_K).  Validates the
  * sizes, dtypes and layout like hgemm_run (pointers are not involved).
  */
 hgemm_status_t hgemm_plan(int64_t M, int64_t N, int64_t K, hgemm_layout_t layout, hgemm_dtype_t in_dtype,
@@ -386,14 +398,15 @@ uint64_t hgemm_encode_smem_desc(uint32_t smem_addr, uint32_t lbo_bytes, uint32_t
  * or allocating library routine is called.
  *   A: device pointer, M x K row-major; B: device pointer, N x K row-major
  *   (TN); C: device pointer, M x N row-major, written.  The caller owns all three.
- *   Limits: 1 <= M <= 64 and N <= 33,554,432 (two counters for each of the
- *   ceil(N/128) tiles fit in 2 MiB); larger sizes return
- *   HGEMM_ERR_UNSUPPORTED.  M == 0 or N == 0 is a no-op; K == 0 writes +0.  Alignment and aliasing rules are those of
+ *   Limits: 1 <= M <= 64 and N <= 67,108,864 (one arrival counter for each
+ *   of the ceil(N/128) tiles, in a 2 MiB part of the array); larger sizes
+ *   return HGEMM_ERR_UNSUPPORTED.  M == 0 or N == 0 is a no-op; K == 0 writes +0.  Alignment and aliasing rules are those of
  *   hgemm_run (HGEMM_ERR_MISALIGNED, HGEMM_ERR_ALIAS, HGEMM_ERR_INVALID_ARG).
  *   in_dtype, out_dtype: HGEMM_F16 or HGEMM_BF16.
  * The first call on each device does a one-time set-up with that device
  * current (the array's device address, the SM count, the kernel's shared-
- * memory limit); make that first call before any stream capture.  Every call
+ * memory limit); make that first call before any stream capture.  A set-up
+ * that fails returns its error and is tried again by the next call.  Every call
  * clears the status word and the tickets it uses, on `stream`, before the
  * kernel.  All calls on a device share the one array, so calls whose kernels
  * overlap on the GPU (different streams without ordering) race and give

@@ -258,11 +258,13 @@ static void* entries_worker(void* arg) {
 }
 
 /* Computes the double dot products for entries (rows[i], cols[i]), i < count.
- * Indices must lie inside [0,M) x [0,N).  Returns 0, or -1 on bad arguments. */
+ * Indices must lie inside [0,M) x [0,N) and layout must be TN or NN.
+ * Returns 0, or -1 on bad arguments (nothing is written then).             */
 int oracle_gemm_entries(const uint16_t* A, const uint16_t* B, int64_t M, int64_t N, int64_t K,
                         int layout, int in_dtype, const int64_t* rows, const int64_t* cols,
                         int64_t count, double* exact, double* absdot, int nthreads) {
   if (M < 0 || N < 0 || K < 0 || count < 0) return -1;
+  if (layout != OR_TN && layout != OR_NN) return -1;
   for (int64_t i = 0; i < count; i++)
     if (rows[i] < 0 || rows[i] >= M || cols[i] < 0 || cols[i] >= N) return -1;
   double* lut = make_lut(in_dtype);
@@ -311,6 +313,7 @@ int oracle_gemm_tiled(const uint16_t* A, const uint16_t* B, int64_t M, int64_t N
                       int layout, int in_dtype, int64_t BM, int64_t BN, int64_t BK,
                       double* C_exact) {
   if (M < 0 || N < 0 || K < 0 || BM <= 0 || BN <= 0 || BK <= 0) return -1;
+  if (layout != OR_TN && layout != OR_NN) return -1;
   double* lut = make_lut(in_dtype);
   if (!lut) return -1;
   double* acc = (double*)malloc(sizeof(double) * BM * BN);

@@ -50,6 +50,7 @@ struct Ctx {
   int stream_k = 1;  // 0 never, 1 when the estimate says so, 2 whenever the tile count leaves a partial wave
   int schedule = HGEMM_SCHEDULE_STATIC;
   int epilogue = HGEMM_EPILOGUE_TMA_STORE;
+  int pdl_prefetch = 0;  // dense: k-blocks of the first item prefetched before the wait on the previous grid
   bool checks = false;
   TraceBuf* trace = nullptr;  // device trace buffer (HGEMM_OPT_TRACE)
   int64_t trace_capacity = 0;
@@ -144,6 +145,8 @@ struct DenseChoice {
   int clusters;       // persistent clusters launched
   int dp_tiles;       // tiles computed whole
   int64_t sk_units;   // k-block units of the stream-K range
+  int sk_ranges;      // stream-K work ids (0 without stream-K)
+  int sk_pieces;      // 0: one equal range per cluster; p: each split tile cut into p equal K pieces
 };
 
 // Data-parallel: ceil(T / P) rounds of whole tiles.  Stream-K: the remainder
@@ -164,7 +167,7 @@ DenseChoice dense_choice(DenseKind kind, int64_t M, int64_t N, int64_t K, int ca
   const int64_t kb = cdiv(K, 64);
   int64_t P = capacity > 0 ? capacity : 1;
   if (max_ctas > 0) P = std::max<int64_t>(1, std::min<int64_t>(P, max_ctas / info.cta_group));
-  DenseChoice dp{(double)cdiv(tiles, P), (int)std::min<int64_t>(tiles, P), (int)tiles, 0};
+  DenseChoice dp{(double)cdiv(tiles, P), (int)std::min<int64_t>(tiles, P), (int)tiles, 0, 0, 0};
   DenseChoice best = dp;
   if (allow_sk && kb >= 2 && tiles % P != 0) {
     const int64_t waves = tiles / P;
@@ -173,8 +176,39 @@ DenseChoice dense_choice(DenseKind kind, int64_t M, int64_t N, int64_t K, int ca
     sk.dp_tiles = (int)(waves >= 1 ? (rem * 4 >= P ? waves : waves - 1) * P : 0);
     sk.sk_units = (tiles - sk.dp_tiles) * kb;
     sk.clusters = (int)std::min<int64_t>(P, sk.sk_units);
+    sk.sk_ranges = sk.clusters;
+    sk.sk_pieces = 0;
     sk.cost = (double)tiles / (double)sk.clusters + 30.0 / (double)kb;
-    if (sk.cost < dp.cost || allow_sk == 2) best = sk;
+    // K pieces: each of the rem leftover tiles is cut into p = P / rem equal
+    // K pieces, one per cluster.  All pieces start together, the first
+    // pieces of every split tile at k = 0, the second ones at k = kb / p, ...,
+    // so the clusters walk K side by side and share each A and B line fetch
+    // the way a wave of whole tiles does; equal ranges per cluster start at
+    // scattered K offsets and fetch nearly every line alone.  The price: the
+    // makespan is ceil(kb / p) instead of rem * kb / P k-blocks.
+    // At most kMaxPieces contributors per split tile: every further one adds
+    // a published fp32 partial to the tile's fix-up.
+    DenseChoice pc{};
+    constexpr int64_t kMaxPieces = 4;
+    const int64_t pieces = rem > 0 ? std::min<int64_t>(std::min<int64_t>(P / rem, kb), kMaxPieces) : 0;
+    if (pieces >= 2 || (allow_sk == 3 && kb >= 2)) {
+      pc.sk_pieces = (int)std::max<int64_t>(2, pieces);
+      pc.dp_tiles = (int)(waves * P);
+      pc.sk_units = rem * kb;
+      pc.sk_ranges = (int)(rem * pc.sk_pieces);
+      pc.clusters = (int)std::min<int64_t>(P, std::max<int64_t>(pc.dp_tiles, pc.sk_ranges));
+      // The fix-ups of split tiles run under the whole tiles' mainloops when
+      // there are whole tiles; they still cost their partial traffic.
+      pc.cost = (double)waves + (double)cdiv(kb, pc.sk_pieces) / (double)kb + (waves >= 1 ? 8.0 : 30.0) / (double)kb;
+    }
+    if (allow_sk == 2) {
+      best = sk;
+    } else if (allow_sk == 3) {
+      best = pc.sk_pieces ? pc : sk;
+    } else {
+      if (sk.cost < best.cost) best = sk;
+      if (pc.sk_pieces && pc.cost < best.cost) best = pc;
+    }
   }
   // relative mainloop efficiency per tile area (2-SM 256-wide tiles are the reference)
   const double eff = (kind == kDense2Sm256) ? 1.0 : (kind == kDense2Sm192 ? 0.78 : (kind == kDense1Sm256 ? 0.85 : 0.70));
@@ -202,10 +236,12 @@ void fill_dense_plan(DenseKind kind, const DenseChoice& ch, int64_t M, int64_t N
   p->dp_tiles = ch.dp_tiles;
   p->sk_units = ch.sk_units;
   p->stream_k = ch.sk_units > 0 ? 1 : 0;
-  p->sk_ranges = p->stream_k ? ch.clusters : 0;
+  p->sk_ranges = p->stream_k ? ch.sk_ranges : 0;
+  p->sk_pieces = p->stream_k ? ch.sk_pieces : 0;
   p->work_ids = p->sk_ranges + ch.dp_tiles;
+  // partial slots: two per stream-K range (ranges may outnumber the clusters when pieces are forced)
   p->workspace_bytes =
-      p->stream_k ? (int64_t)ch.clusters * 2 * info.cta_group * info.block_n * 128 * 4 +
+      p->stream_k ? (int64_t)std::max(ch.clusters, ch.sk_ranges) * 2 * info.cta_group * info.block_n * 128 * 4 +
                         (int64_t)p->num_tiles * info.cta_group * 8
                   : 0;
 }
@@ -244,7 +280,8 @@ hgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int layout, int in, in
     p->tiles_n = 1;
     p->num_tiles = p->tiles_m;
     p->k_blocks = (int32_t)cdiv(K, kSplitKBlockK);
-    const SplitKShape sh = splitk_shape(p->num_tiles, p->k_blocks, K, mma_n, num_sms, max_ctas, optin, allow_sk,
+    const SplitKShape sh = splitk_shape(p->num_tiles, p->k_blocks, K, mma_n, num_sms, max_ctas, optin,
+                                        allow_sk == 3 ? 2 : allow_sk,
                                         schedule == HGEMM_SCHEDULE_DYNAMIC);
     p->stages = sh.stages;
     p->grid = sh.ctas;
@@ -386,7 +423,7 @@ uint64_t hgemm_encode_smem_desc(uint32_t smem_addr, uint32_t lbo_bytes, uint32_t
 hgemm_status_t hgemm_plan_ex(int64_t M, int64_t N, int64_t K, hgemm_layout_t layout, hgemm_dtype_t in_dtype,
                              hgemm_dtype_t acc_dtype, hgemm_dtype_t out_dtype, int32_t num_sms, int32_t variant,
                              int32_t group_m, int32_t stream_k, int32_t schedule, hgemm_plan_t* plan) {
-  if (!plan || group_m < 0 || stream_k < 0 || stream_k > 2) return HGEMM_ERR_INVALID_ARG;
+  if (!plan || group_m < 0 || stream_k < 0 || stream_k > 3) return HGEMM_ERR_INVALID_ARG;
   return make_plan(M, N, K, layout, in_dtype, acc_dtype, out_dtype, num_sms, kDefaultSmemOptin, nullptr, variant,
                    group_m, 0, stream_k, schedule, plan);
 }
@@ -567,7 +604,7 @@ hgemm_status_t hgemm_set_option(hgemm_handle_t h, int32_t option, int64_t value)
       h->max_ctas = (int)value;
       return HGEMM_OK;
     case HGEMM_OPT_STREAM_K:
-      if (value < 0 || value > 2) return HGEMM_ERR_INVALID_ARG;
+      if (value < 0 || value > 3) return HGEMM_ERR_INVALID_ARG;
       h->stream_k = (int)value;
       return HGEMM_OK;
     case HGEMM_OPT_SCHEDULE:
@@ -581,6 +618,10 @@ hgemm_status_t hgemm_set_option(hgemm_handle_t h, int32_t option, int64_t value)
     case HGEMM_OPT_EPILOGUE:
       if (value != HGEMM_EPILOGUE_TMA_STORE && value != HGEMM_EPILOGUE_DIRECT) return HGEMM_ERR_INVALID_ARG;
       h->epilogue = (int)value;
+      return HGEMM_OK;
+    case HGEMM_OPT_PDL_PREFETCH:
+      if (value < 0 || value > 64) return HGEMM_ERR_INVALID_ARG;
+      h->pdl_prefetch = (int)value;
       return HGEMM_OK;
     case HGEMM_OPT_TRACE: {
       if (value < 0 || value > (int64_t)1 << 26) return HGEMM_ERR_INVALID_ARG;
@@ -696,6 +737,7 @@ hgemm_status_t hgemm_run(hgemm_handle_t h, const void* A, const void* B, void* C
   args.acc_f16 = acc_dtype == HGEMM_F16;
   args.out_bf16 = out_dtype == HGEMM_BF16;
   args.inject = h->inject;
+  args.pdl_prefetch = h->pdl_prefetch;
   args.timeout_ns = h->timeout_ns;
   args.status = h->status;
   args.trace = h->trace;
@@ -709,8 +751,9 @@ hgemm_status_t hgemm_run(hgemm_handle_t h, const void* A, const void* B, void* C
   args.partials = nullptr;
   args.tickets = nullptr;
   if (p.stream_k) {
-    const size_t clusters = (size_t)(p.grid / info.cta_group);
-    const size_t partial_bytes = clusters * 2 * (size_t)info.cta_group * (size_t)info.block_n * 128 * sizeof(float);
+    // two partial slots per stream-K range (the kernel indexes them by range id)
+    const size_t ranges = (size_t)std::max(p.grid / info.cta_group, p.sk_ranges);
+    const size_t partial_bytes = ranges * 2 * (size_t)info.cta_group * (size_t)info.block_n * 128 * sizeof(float);
     // two counters per tile and CTA of the pair: arrivals, then publications
     st = ensure_workspace(h, partial_bytes, (size_t)p.num_tiles * (size_t)info.cta_group * 2, s);
     if (st != HGEMM_OK) return st;

@@ -29,7 +29,11 @@ namespace {
 // Scratch layout: [status word | per-tile tickets | fp32 partial sums].
 constexpr size_t kNoAllocScratchBytes = (size_t)16 << 20;  // 16 MiB
 constexpr size_t kStatusBytes = 256;
-constexpr size_t kTicketBytes = (size_t)2 << 20;  // N <= 33,554,432; one counter per line up to 16384 tiles
+// One arrival counter per N tile (the split-K kernel keeps no other per-tile
+// state): 2 MiB holds 524,288 counters, so N <= 67,108,864.  Counters sit one
+// per 128-byte line while that fits (up to 16,384 tiles), else packed.
+constexpr size_t kTicketBytes = (size_t)2 << 20;
+constexpr int64_t kMaxN = (int64_t)(kTicketBytes / sizeof(int32_t)) * 128;
 constexpr size_t kPartialOffset = kStatusBytes + kTicketBytes;
 constexpr size_t kPartialBytes = kNoAllocScratchBytes - kPartialOffset;
 constexpr int kMaxDevices = 64;
@@ -43,7 +47,8 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 namespace {
 
 struct DeviceSetup {
-  std::once_flag once;
+  std::mutex mu;
+  bool done = false;  // set only by a set-up that succeeded; a failed one is retried by the next call
   hgemm_status_t status = HGEMM_ERR_NO_DEVICE;
   unsigned char* scratch = nullptr;  // device address of g_noalloc_scratch
   int sm_count = 0;
@@ -52,7 +57,7 @@ struct DeviceSetup {
 
 DeviceSetup g_devices[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_noalloc_encode = nullptr;
-std::once_flag g_noalloc_encode_once;
+std::mutex g_noalloc_encode_mu;
 
 void load_encode_fn() {
   void* fn = nullptr;
@@ -120,8 +125,8 @@ extern "C" hgemm_status_t hgemm_run_splitk_noalloc(const void* A, const void* B,
   if (in_dtype == HGEMM_F32 || out_dtype == HGEMM_F32) return HGEMM_ERR_UNSUPPORTED;
   if (M == 0 || N == 0) return HGEMM_OK;
   if (M > hg::kSplitKMaxM) return HGEMM_ERR_UNSUPPORTED;  // beyond the scratch layout's maximum
+  if (N > kMaxN) return HGEMM_ERR_UNSUPPORTED;  // one ticket per 128-column tile must fit the ticket area
   const int64_t n_tiles = (N + 127) / 128;
-  if ((size_t)n_tiles * 2 * sizeof(int32_t) > kTicketBytes) return HGEMM_ERR_UNSUPPORTED;
   if (N % 8 != 0 || (K > 0 && K % 8 != 0)) return HGEMM_ERR_MISALIGNED;
   if (!C || (K > 0 && (!A || !B))) return HGEMM_ERR_INVALID_ARG;
   const uintptr_t a = reinterpret_cast<uintptr_t>(A), b = reinterpret_cast<uintptr_t>(B),
@@ -135,10 +140,22 @@ extern "C" hgemm_status_t hgemm_run_splitk_noalloc(const void* A, const void* B,
   if (cudaGetDevice(&dev) != cudaSuccess) return HGEMM_ERR_NO_DEVICE;
   if (dev < 0 || dev >= kMaxDevices) return HGEMM_ERR_UNSUPPORTED;
   DeviceSetup* d = &g_devices[dev];
-  std::call_once(d->once, setup_device, d, dev);
-  if (d->status != HGEMM_OK) return d->status;
-  std::call_once(g_noalloc_encode_once, load_encode_fn);
-  if (!g_noalloc_encode) return HGEMM_ERR_NO_DEVICE;
+  {
+    // Once per device, with that device current.  A set-up that failed (a
+    // sticky error left by earlier work, say) is not remembered: the next call
+    // tries again.
+    std::lock_guard<std::mutex> lock(d->mu);
+    if (!d->done) {
+      setup_device(d, dev);
+      d->done = d->status == HGEMM_OK;
+    }
+    if (!d->done) return d->status;
+  }
+  {
+    std::lock_guard<std::mutex> lock(g_noalloc_encode_mu);
+    if (!g_noalloc_encode) load_encode_fn();  // retried while it fails
+    if (!g_noalloc_encode) return HGEMM_ERR_NO_DEVICE;
+  }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (K == 0) return hg::fill_zero_launch(C, c_bytes, s) == cudaSuccess ? HGEMM_OK : HGEMM_ERR_CUDA;
 

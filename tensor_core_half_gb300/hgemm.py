@@ -67,6 +67,7 @@ HGEMM_EPILOGUE_TMA_STORE = 0
 HGEMM_EPILOGUE_DIRECT = 1
 EPILOGUES = {"tma": HGEMM_EPILOGUE_TMA_STORE, "direct": HGEMM_EPILOGUE_DIRECT}
 HGEMM_OPT_CHECKS = 10
+HGEMM_OPT_PDL_PREFETCH = 12
 HGEMM_ERR_CHECK = 9
 HGEMM_CHECK_WORK_ID, HGEMM_CHECK_ITEM, HGEMM_CHECK_TICKET, HGEMM_CHECK_CONTRIBUTOR, HGEMM_CHECK_PARTIAL = 1, 2, 3, 4, 5
 
@@ -83,7 +84,7 @@ class hgemm_plan_t(ctypes.Structure):
         ("workspace_bytes", ctypes.c_int64), ("dp_tiles", ctypes.c_int32), ("stream_k", ctypes.c_int32),
         ("sk_units", ctypes.c_int64), ("sk_ranges", ctypes.c_int32), ("work_ids", ctypes.c_int32),
         ("schedule", ctypes.c_int32), ("splitk_chunks", ctypes.c_int32), ("splitk_head_units", ctypes.c_int64),
-        ("splitk_align", ctypes.c_int32)]
+        ("splitk_align", ctypes.c_int32), ("sk_pieces", ctypes.c_int32)]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}

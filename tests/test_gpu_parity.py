@@ -273,33 +273,55 @@ def test_variants_agree_bitwise(h, layout):
         assert np.array_equal(o, outs[0])
 
 
+@pytest.mark.parametrize("stream_k", [1, 3], ids=["auto", "pieces"])
 @pytest.mark.parametrize("variant", DENSE_VARIANTS)
 @pytest.mark.parametrize("layout", ["TN", "NN"])
 @pytest.mark.parametrize("combo", [("bf16", "f32", "bf16"), ("f16", "f16", "f16")], ids=["bf16", "f16acc"])
 @pytest.mark.parametrize("M,N,K", [(1024, 1280, 1024), (768, 520, 4104), (256, 264, 200)])
-def test_stream_k_parity(h, M, N, K, combo, layout, variant):
-    # Tile counts that leave a partial last wave, so stream-K splits tiles.
+def test_stream_k_parity(h, M, N, K, combo, layout, variant, stream_k):
+    # Tile counts that leave a partial last wave, so stream-K splits tiles
+    # (the estimate's choice, or every leftover tile cut into equal K pieces).
     fin, acc, out = combo
     st, p = hgemm.hgemm_plan(M, N, K, hgemm.LAYOUTS[layout], hgemm.DTYPES[fin], hgemm.DTYPES[acc], hgemm.DTYPES[out],
-                             torch.cuda.get_device_properties(0).multi_processor_count, hgemm.VARIANTS[variant])
+                             torch.cuda.get_device_properties(0).multi_processor_count, hgemm.VARIANTS[variant], 0,
+                             stream_k)
     if layout == "NN" and variant in NN_UNSUPPORTED:
         assert st == hgemm.HGEMM_ERR_UNSUPPORTED
         pytest.skip("variant %s does not take the NN layout" % variant)
     assert st == 0
+    if stream_k == 3:
+        assert p.stream_k and p.sk_pieces >= 2
     a, b, ab, bb = parity.inputs(M, N, K, layout, fin, ("uniform", -1.0, 1.0), 61)
-    got = run(h, a, b, M, N, K, layout, acc, out, variant)
+    got = run(h, a, b, M, N, K, layout, acc, out, variant, stream_k=stream_k)
     parity.check(got, ab, bb, M, N, K, layout, fin, acc, out)
-    again = run(h, a, b, M, N, K, layout, acc, out, variant)
+    again = run(h, a, b, M, N, K, layout, acc, out, variant, stream_k=stream_k)
     assert np.array_equal(got, again)  # the fix-up order is fixed: run-to-run identical
 
 
+@pytest.mark.parametrize("stream_k", [1, 2, 3], ids=["auto", "ranges", "pieces"])
 @pytest.mark.parametrize("variant", DENSE_VARIANTS)
-def test_stream_k_small_integers_bit_exact(h, variant):
+def test_stream_k_small_integers_bit_exact(h, variant, stream_k):
     M, N, K = 640, 640, 4096
     a, b, ab, bb = parity.inputs(M, N, K, "TN", "bf16", ("int", -4, 4), 62)
-    got = run(h, a, b, M, N, K, "TN", "f32", "bf16", variant)
+    got = run(h, a, b, M, N, K, "TN", "f32", "bf16", variant, stream_k=stream_k)
     ref, _, _ = oracle.gemm(ab, bb, M, N, K, "TN", "bf16", "bf16")
     assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("M,N,K", [(4096, 4096, 2048), (4096, 5120, 1024), (2560, 9984, 768)])
+def test_stream_k_pieces_at_wave_scale(h, M, N, K):
+    """Shapes with whole waves plus leftover tiles, planned the way the
+    headline is (whole waves of 256 x 256 tiles, each leftover tile cut into
+    2 to 4 equal K pieces): sampled parity against the oracle and run-to-run
+    identity, for the estimate's plan and for equal ranges per cluster."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    st, p = hgemm.hgemm_plan(M, N, K, num_sms=sms)
+    assert st == 0 and p.stream_k and p.sk_pieces >= 2 and p.dp_tiles > 0
+    a, b, ab, bb = parity.inputs(M, N, K, "TN", "bf16", ("normal", 1.0), 63)
+    for sk in (1, 2):
+        got = run(h, a, b, M, N, K, "TN", "f32", "bf16", stream_k=sk)
+        parity.check(got, ab, bb, M, N, K, "TN", "bf16", "f32", "bf16", sampled=True)
+        assert np.array_equal(got, run(h, a, b, M, N, K, "TN", "f32", "bf16", stream_k=sk))
 
 
 # Dynamic schedule (cluster launch control).  Shapes with more work ids than
@@ -307,7 +329,8 @@ def test_stream_k_small_integers_bit_exact(h, variant):
 # their ids, with and without stream-K ranges; plus a ragged shape.
 DYNAMIC_CASES = [("2sm256", 4096, 4096, 128, 1), ("2sm256", 4096, 4096, 128, 0), ("1sm128", 2048, 2048, 256, 0),
                  ("1sm256", 2048, 4096, 192, 1), ("2sm192", 2048, 3072, 136, 1), ("2sm256", 1000, 3000, 4104, 1),
-                 ("1sm128", 130, 136, 72, 1)]
+                 ("1sm128", 130, 136, 72, 1), ("2sm256", 4096, 4096, 1024, 3), ("2sm256", 4096, 4096, 256, 2),
+                 ("1sm128", 1000, 3000, 520, 3)]
 
 
 @pytest.mark.parametrize("variant,M,N,K,sk", DYNAMIC_CASES)

@@ -71,8 +71,9 @@ def test_plan_variant_choice():
     assert st == ST_OK and p.variant == H.HGEMM_VARIANT_2SM_256x256 and p.cta_group == 2
     assert (p.tile_m, p.tile_n, p.tiles_m, p.tiles_n, p.num_tiles, p.k_blocks) == (256, 256, 16, 16, 256, 64)
     assert p.grid == 152 and p.tmem_cols == 512 and p.smem_bytes <= 232448
-    # 256 tiles over 76 pairs: two whole waves data-parallel, the rest stream-K
-    assert p.stream_k == 1 and p.dp_tiles == 228 and p.sk_units == (256 - 228) * 64  # remainder of 28 tiles split
+    # 256 tiles over 76 pairs: three whole waves data-parallel, the remaining
+    # 28 tiles each cut into 2 K pieces
+    assert p.stream_k == 1 and p.dp_tiles == 228 and p.sk_units == (256 - 228) * 64 and p.sk_pieces == 2
     st, p = plan(4096, 4096, 4096, stream_k=0, variant=3)
     assert st == ST_OK and p.stream_k == 0 and p.dp_tiles == 256 and p.sk_units == 0 and p.workspace_bytes == 0
     # a tile count that is a whole number of waves stays data-parallel
@@ -309,14 +310,29 @@ def test_work_lists_cover_every_unit_once(M, N, K, variant):
             i += 1
         per_cluster.append(work)
     assert len(covered) == p.num_tiles * p.k_blocks
-    if p.stream_k:
-        # every cluster does the same number of k-blocks, up to one
+    if p.stream_k and p.sk_pieces == 0:
+        # equal ranges: every cluster does the same number of k-blocks, up to one
         assert max(per_cluster) - min(per_cluster) <= 1
         # a split tile's pieces come from consecutive clusters, in K order
         for t in range(p.dp_tiles, p.num_tiles):
             owners = [covered[(t, kb)] for kb in range(p.k_blocks)]
             assert owners == sorted(owners)
             assert set(owners) == set(range(owners[0], owners[-1] + 1))
+    if p.stream_k and p.sk_pieces:
+        # K pieces: each split tile is cut into sk_pieces pieces of equal
+        # length (up to one k-block) that start at the same K offsets in
+        # every split tile, one piece per cluster
+        piece = -(-p.k_blocks // p.sk_pieces)
+        starts = None
+        for t in range(p.dp_tiles, p.num_tiles):
+            owners = [covered[(t, kb)] for kb in range(p.k_blocks)]
+            cuts = [0] + [kb for kb in range(1, p.k_blocks) if owners[kb] != owners[kb - 1]]
+            assert len(cuts) == p.sk_pieces and len(set(owners)) == p.sk_pieces
+            starts = starts or cuts
+            assert cuts == starts
+            lens = [b - a for a, b in zip(cuts, cuts[1:] + [p.k_blocks])]
+            assert max(lens) - min(lens) <= 1
+        assert max(per_cluster) - min(per_cluster) <= piece
 
 
 @pytest.mark.parametrize("M,N,K,variant", STREAMK_CASES)
@@ -329,7 +345,12 @@ def test_work_ids_partition_the_work(M, N, K, variant):
     assert st == ST_OK
     clusters = p.grid // p.cta_group
     assert p.work_ids == p.sk_ranges + p.dp_tiles
-    assert p.sk_ranges == (clusters if p.stream_k else 0)
+    if not p.stream_k:
+        assert p.sk_ranges == 0
+    elif p.sk_pieces == 0:
+        assert p.sk_ranges == clusters
+    else:
+        assert p.sk_ranges == (p.num_tiles - p.dp_tiles) * p.sk_pieces <= clusters
     items = {}
     covered = set()
     for i in range(p.work_ids):
@@ -405,13 +426,23 @@ def test_tma_bench_reference_sums():
 
 
 def test_stream_k_split_by_remainder():
-    # 2-SM 256 x 256 tiles, 76 pairs.  86 tiles: a remainder of 10 (< 76 / 4)
-    # would be cut among ~8 pairs each, so the whole first round joins the split.
-    st, p = plan(512, 256 * 43, 4096, variant=3)
+    # 2-SM 256 x 256 tiles, 76 pairs.  Equal ranges (stream_k = 2), 86 tiles: a
+    # remainder of 10 (< 76 / 4) would be cut among ~8 pairs each, so the whole
+    # first round joins the split.
+    st, p = plan(512, 256 * 43, 4096, variant=3, stream_k=2)
     assert st == ST_OK and p.num_tiles == 86 and p.stream_k == 1 and p.dp_tiles == 0 and p.sk_units == 86 * 64
+    assert p.sk_pieces == 0 and p.sk_ranges == 76
     # 106 tiles: a remainder of 30 (>= 19) is split alone; 76 tiles stay whole.
-    st, p = plan(512, 256 * 53, 4096, variant=3)
+    st, p = plan(512, 256 * 53, 4096, variant=3, stream_k=2)
     assert st == ST_OK and p.num_tiles == 106 and p.stream_k == 1 and p.dp_tiles == 76 and p.sk_units == 30 * 64
+    # The estimate's choice: K pieces.  A remainder of 10 tiles is cut into 4
+    # pieces each (76 / 10 = 7, capped at 4), 30 tiles into 2 pieces each;
+    # the first round stays whole.
+    st, p = plan(512, 256 * 43, 4096, variant=3)
+    assert st == ST_OK and p.stream_k == 1 and p.dp_tiles == 76 and p.sk_units == 10 * 64
+    assert p.sk_pieces == 4 and p.sk_ranges == 40 and p.grid == 152
+    st, p = plan(512, 256 * 53, 4096, variant=3)
+    assert st == ST_OK and p.dp_tiles == 76 and p.sk_pieces == 2 and p.sk_ranges == 60
 
 
 def test_stream_k_option_values():
@@ -422,8 +453,16 @@ def test_stream_k_option_values():
     st, p = plan(1000, 3000, 4104, variant=3, stream_k=2)
     assert st == ST_OK and p.stream_k == 1 and p.dp_tiles == 0 and p.sk_units == 48 * 65
     st, p = plan(4096, 4096, 4096, variant=3, stream_k=2)
-    assert st == ST_OK and p.stream_k == 1 and p.dp_tiles == 228  # same split as the estimate picks
+    assert st == ST_OK and p.stream_k == 1 and p.dp_tiles == 228 and p.sk_pieces == 0 and p.sk_ranges == 76
+    # 3: K pieces (the estimate's choice here): 28 leftover tiles, 2 pieces each
     st, p = plan(4096, 4096, 4096, variant=3, stream_k=3)
+    assert st == ST_OK and p.stream_k == 1 and p.dp_tiles == 228 and p.sk_pieces == 2 and p.sk_ranges == 56
+    st, q = plan(4096, 4096, 4096, variant=3, stream_k=1)
+    assert (q.dp_tiles, q.sk_units, q.sk_ranges, q.sk_pieces) == (228, 28 * 64, 56, 2)
+    # 48 tiles for 76 pairs: one piece per tile fits, so 3 forces two
+    st, p = plan(1000, 3000, 4104, variant=3, stream_k=3)
+    assert st == ST_OK and p.dp_tiles == 0 and p.sk_pieces == 2 and p.sk_ranges == 96 and p.grid == 152
+    st, p = plan(4096, 4096, 4096, variant=3, stream_k=4)
     assert st == ST_INV
 
 
@@ -507,3 +546,20 @@ def test_tile_count_beyond_32_bits_is_rejected():
     assert st == ST_OK
     st, _ = H.hgemm_plan(128 * 46341, 128 * 46341, 64, num_sms=152)   # 46341^2 > 2^31 - 1
     assert st == H.HGEMM_ERR_INVALID_ARG
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
+def test_noalloc_size_limit_at_its_boundary():
+    """The allocation-free entry point keeps one arrival counter per 128-column
+    tile in a 2 MiB area: N up to 67,108,864 passes the size check (and then
+    finds no device here); one more tile's worth is refused before any device
+    call.  The pointers are never dereferenced."""
+    R = H.hgemm_run_splitk_noalloc
+    bf = H.HGEMM_BF16
+    A, B, C = 1 << 40, 2 << 40, 3 << 40
+    n_max = (2 << 20) // 4 * 128
+    assert n_max == 67108864
+    assert R(A, B, C, 16, n_max + 8, 64, bf, bf, 0) == ST_UNS
+    assert R(A, B, C, 16, n_max, 64, bf, bf, 0) == H.HGEMM_ERR_NO_DEVICE
+    assert R(A, B, C, 64, 64, 64, bf, bf, 0) == H.HGEMM_ERR_NO_DEVICE
+    assert R(A, B, C, 65, 64, 64, bf, bf, 0) == ST_UNS

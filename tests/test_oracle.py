@@ -335,3 +335,37 @@ def test_bad_entry_index_is_rejected():
     A = _enc(np.ones((2, 2)), "f16")
     with pytest.raises(RuntimeError):
         oracle.gemm_entries(A, A, 2, 2, 2, "TN", "f16", [0, 2], [0, 0])
+
+
+@pytest.mark.parametrize("layout", [-1, 2, 7])
+def test_bad_layout_is_rejected_by_the_c_entry_points(layout):
+    """The C functions themselves refuse a layout that is neither TN nor NN
+    (the Python wrapper checks too, but a caller of the library must not get
+    B silently read as NN), and leave the outputs untouched."""
+    import ctypes
+    lib = oracle._load()
+    A = _enc(np.ones((2, 3)), "f16")
+    u16p = ctypes.POINTER(ctypes.c_uint16)
+    f64p = ctypes.POINTER(ctypes.c_double)
+    i64p = ctypes.POINTER(ctypes.c_int64)
+    rows = np.array([0, 1], np.int64)
+    cols = np.array([1, 0], np.int64)
+    ex = np.full(2, 7.0)
+    ab = np.full(2, 7.0)
+    st = lib.oracle_gemm_entries(A.ctypes.data_as(u16p), A.ctypes.data_as(u16p), 2, 2, 3, layout, 0,
+                                 rows.ctypes.data_as(i64p), cols.ctypes.data_as(i64p), 2, ex.ctypes.data_as(f64p),
+                                 ab.ctypes.data_as(f64p), 1)
+    assert st == -1 and np.all(ex == 7.0) and np.all(ab == 7.0)
+    C = np.zeros(4, np.uint16)
+    full = np.full(4, 7.0)
+    st = lib.oracle_gemm(A.ctypes.data_as(u16p), A.ctypes.data_as(u16p), 2, 2, 3, layout, 0, 0,
+                         C.ctypes.data_as(u16p), full.ctypes.data_as(f64p), None, 1)
+    assert st == -1 and np.all(full == 7.0)
+    st = lib.oracle_gemm_tiled(A.ctypes.data_as(u16p), A.ctypes.data_as(u16p), 2, 2, 3, layout, 0, 1, 1, 1,
+                               full.ctypes.data_as(f64p))
+    assert st == -1 and np.all(full == 7.0)
+    # the same call with a valid layout succeeds
+    st = lib.oracle_gemm_entries(A.ctypes.data_as(u16p), A.ctypes.data_as(u16p), 2, 2, 3, 0, 0,
+                                 rows.ctypes.data_as(i64p), cols.ctypes.data_as(i64p), 2, ex.ctypes.data_as(f64p),
+                                 ab.ctypes.data_as(f64p), 1)
+    assert st == 0 and np.all(ex == 3.0) and np.all(ab == 3.0)

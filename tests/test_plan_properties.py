@@ -22,7 +22,7 @@ def _dense_cases(n, seed):
         K = int(8 * r.integers(1, 1200))
         sms = int(r.choice([8, 16, 40, 76, 132, 148, 152]))
         variant = int(r.choice([1, 2, 3, 5]))
-        stream_k = int(r.choice([0, 1, 2]))
+        stream_k = int(r.choice([0, 1, 2, 3]))
         yield M, N, K, sms, variant, stream_k
 
 
@@ -57,6 +57,12 @@ def test_dense_work_ids_partition_units(seed):
         if p.sk_ranges:
             sk = id_kb[:p.sk_ranges]
             assert max(sk) - min(sk) <= 1  # equal stream-K ranges
+            # the kernel keeps two fp32 partial slots [cta_group][tile_n][128]
+            # per range id: the workspace the plan asks for must hold them all
+            slots = 2 * p.sk_ranges * p.cta_group * p.tile_n * 128 * 4
+            assert p.workspace_bytes >= slots + p.num_tiles * p.cta_group * 8
+        if p.sk_pieces:
+            assert 2 <= p.sk_pieces <= 4 and p.sk_ranges == (p.num_tiles - p.dp_tiles) * p.sk_pieces
         # the static walk of every cluster: ids c, c + P, ... and nothing else
         per_cluster = []
         for c in range(clusters):
@@ -70,7 +76,7 @@ def test_dense_work_ids_partition_units(seed):
             assert kb == sum(id_kb[c::clusters])
             per_cluster.append(kb)
         if p.sk_ranges:  # stream-K evens the work out
-            assert max(per_cluster) - min(per_cluster) <= p.k_blocks
+            assert max(per_cluster) - min(per_cluster) <= p.k_blocks + 1
 
 
 @pytest.mark.parametrize("seed", range(4))

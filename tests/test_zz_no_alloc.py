@@ -67,6 +67,9 @@ def test_noalloc_rejects_sizes_beyond_its_maximum():
     bf = hgemm.HGEMM_BF16
     assert R(A.data_ptr(), B.data_ptr(), C.data_ptr(), 65, 64, 64, bf, bf, s) == hgemm.HGEMM_ERR_UNSUPPORTED
     assert R(A.data_ptr(), B.data_ptr(), C.data_ptr(), 16, 1 << 30, 64, bf, bf, s) == hgemm.HGEMM_ERR_UNSUPPORTED
+    # one arrival counter per 128-column tile fits 2 MiB up to N = 67,108,864
+    assert R(A.data_ptr(), B.data_ptr(), C.data_ptr(), 16, 67108864 + 8, 64, bf, bf, s) == \
+        hgemm.HGEMM_ERR_UNSUPPORTED
     assert R(A.data_ptr(), B.data_ptr(), C.data_ptr(), 16, 60, 64, bf, bf, s) == hgemm.HGEMM_ERR_MISALIGNED
     assert R(A.data_ptr(), B.data_ptr(), A.data_ptr(), 16, 64, 64, bf, bf, s) == hgemm.HGEMM_ERR_ALIAS
     assert R(0, B.data_ptr(), C.data_ptr(), 16, 64, 64, bf, bf, s) == hgemm.HGEMM_ERR_INVALID_ARG
