@@ -17,6 +17,13 @@ device->host copy of C inside the timed region; consecutive steps alternate
 between two caller streams (--e2e-streams), so that one step's uploads overlap
 the previous step's GEMM and download.
 
+After the K timed steps (one GPU only; --no-secondary skips them): a
+sustained loop of the same launches lasting >= 1 s, whose clocks the sampler
+does see, against the sustained peak; the other target workloads (8192^3 bf16,
+the skinny 16x16384x8192 product against HBM) and the two weakest shapes
+(1000x3000x4104, 2048^3 fp16), each with its own roofline; and the CPU oracle
+on the 256^3 workload and on 2048^3, one thread and all host cores.
+
 N > 1 (torchrun): independent replicas, one per GPU, each running the full
 workload (weak scaling); the time is the maximum over ranks.
 
@@ -88,7 +95,8 @@ def load_traffic(workload: str, variant: int, plan=None):
         return None
     want = e.get("plan")
     if plan is not None and want is not None:
-        have = {"grid": plan.grid, "dp_tiles": plan.dp_tiles, "sk_units": plan.sk_units}
+        have = {"grid": plan.grid, "dp_tiles": plan.dp_tiles, "sk_units": plan.sk_units,
+                "sk_ranges": plan.sk_ranges}
         if any(have[k] != v for k, v in want.items()):
             return None
     return e.get("dram_bytes_per_launch")
@@ -246,10 +254,11 @@ def host_cpu_model() -> str:
     return "CPU implementer %s, part %s" % (impl[0] if impl else "?", part[0] if part else "?")
 
 
-def oracle_timing():
+def oracle_timing(names=("square256_f16", "sweep2048_f16_accf32"), emit=True):
     """The CPU oracle on the small workloads, one thread and all host cores:
     each a median of 3 full products (one run where a single-threaded product
-    takes over 30 s), GFLOP/s = 2MNK / t.  One JSON line per run."""
+    takes over 30 s), GFLOP/s = 2MNK / t.  Returns one record per run (and
+    prints each as a JSON line when emit is set)."""
     import numpy as np
 
     import oracle
@@ -257,7 +266,8 @@ def oracle_timing():
     cores = os.cpu_count() or 1
     nproc = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else cores
     model = host_cpu_model()
-    for name in ("square256_f16", "sweep2048_f16_accf32"):
+    out = []
+    for name in names:
         w = workloads.WORKLOADS[name]
         a, b = workloads.generate_workload(w)
         ab, bb = workloads.bits(a), workloads.bits(b)
@@ -270,10 +280,103 @@ def oracle_timing():
                 if times[-1] > 30.0:
                     break
             t = float(np.median(times))
-            print(json.dumps({"oracle_timing": name, "M": w.M, "N": w.N, "K": w.K, "in": w.in_dtype,
-                              "threads": threads, "runs": len(times), "seconds": round(t, 4),
-                              "gflops": round(2.0 * w.M * w.N * w.K / t / 1e9, 3), "hardware_concurrency": cores,
-                              "nproc": nproc, "cpu": model}), flush=True)
+            rec = {"oracle_timing": name, "M": w.M, "N": w.N, "K": w.K, "in": w.in_dtype, "threads": threads,
+                   "runs": len(times), "seconds": round(t, 4), "gflops": round(2.0 * w.M * w.N * w.K / t / 1e9, 3),
+                   "hardware_concurrency": cores, "nproc": nproc, "cpu": model}
+            out.append(rec)
+            if emit:
+                print(json.dumps(rec), flush=True)
+    return out
+
+
+def problem_config(w, world):
+    """The workload as both arms name it (the same dict in our line and in the
+    reference arm's line)."""
+    return {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "layout": w.layout, "in": w.in_dtype,
+            "acc": w.acc_dtype, "out": w.out_dtype, "parallelism": "replicas" if world > 1 else "single",
+            "l2": "GPU arm: inputs rotate over copies that together exceed 2x L2, so every launch reads its "
+                  "operands from HBM; CPU oracle arm: host memory"}
+
+
+def roofline_for(w, bound, kernel_ms, peaks, peak_src, sustained):
+    """The roofline object of one kernel: algorithmic work of one launch over
+    its average launch time, against the measured peak of its bound."""
+    if bound == "tensor":
+        peak = peaks.get("bf16_tflops_sustained" if sustained else "bf16_tflops")
+        achieved = (w.flops / 1e12) / (kernel_ms / 1e3)
+        return {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4),
+                "peak_source": "%s %s" % (peak_src, "sustained" if sustained else "burst")}
+    peak = peaks.get("hbm_gbs")
+    achieved = (w.compulsory_bytes / 1e9) / (kernel_ms / 1e3)
+    return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "peak_source": peak_src}
+
+
+def time_workload(w, dev, steps, warmup, n_single, sampler_index=None):
+    """Device-timed launches of one workload through hgemm_run: `steps`
+    back-to-back launches between two events (inputs rotating over copies
+    larger than 2x L2), then the median of `n_single` launches each between
+    its own events.  Returns (ms per launch, median single ms, plan, clocks)."""
+    import torch
+
+    from tensor_core_half_gb300 import hgemm, workloads
+    a_cpu, b_cpu = workloads.generate_workload(w)
+    in_bytes = (a_cpu.numel() + b_cpu.numel()) * 2
+    c_bytes = w.M * w.N * 2
+    copies = max(1, math.ceil(2 * L2_BYTES / max(1, in_bytes + c_bytes)))
+    A = [a_cpu.to(dev) for _ in range(copies)]
+    B = [b_cpu.to(dev) for _ in range(copies)]
+    C = [torch.empty((w.M, w.N), dtype=workloads.DTYPES[w.out_dtype], device=dev) for _ in range(copies)]
+    lay, fin, facc, fout = (hgemm.LAYOUTS[w.layout], hgemm.DTYPES[w.in_dtype], hgemm.DTYPES[w.acc_dtype],
+                            hgemm.DTYPES[w.out_dtype])
+    st, plan = hgemm.hgemm_plan(w.M, w.N, w.K, lay, fin, facc, fout,
+                                torch.cuda.get_device_properties(dev).multi_processor_count)
+    stream = torch.cuda.current_stream(dev)
+    with hgemm.Handle() as h:
+        def step(i):
+            s = hgemm.hgemm_run(h.h, A[i % copies].data_ptr(), B[i % copies].data_ptr(), C[i % copies].data_ptr(),
+                                w.M, w.N, w.K, lay, fin, facc, fout, stream.cuda_stream)
+            if s != hgemm.HGEMM_OK:
+                raise hgemm.HgemmError(s, "hgemm_run (%s)" % w.name)
+
+        for i in range(warmup):
+            step(i)
+        torch.cuda.synchronize(dev)
+        sampler = ClockSampler(sampler_index) if sampler_index is not None else None
+        if sampler:
+            time.sleep(0.25)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        h0 = time.time()
+        e0.record(stream)
+        for i in range(steps):
+            step(i)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        h1 = time.time()
+        clocks = None
+        if sampler:
+            time.sleep(0.1)
+            sampler.stop()
+            clocks = sampler.summary(h0, h1)
+        ms = e0.elapsed_time(e1) / steps
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_single)]
+        for i, (x, y) in enumerate(ev):
+            x.record(stream)
+            step(i)
+            y.record(stream)
+        torch.cuda.synchronize(dev)
+        single = sorted(x.elapsed_time(y) for x, y in ev)
+        st, detail = h.sync_status()
+        if st != hgemm.HGEMM_OK:
+            raise hgemm.HgemmError(st, "%s (detail %s)" % (w.name, hex(detail)))
+    del A, B, C
+    torch.cuda.empty_cache()
+    return ms, single[len(single) // 2], plan, clocks
+
+
+SECONDARY = ("square8192_bf16", "skinny16x16384x8192_bf16", "ragged1000x3000x4104_bf16", "sweep2048_f16_accf32")
 
 
 # ------------------------------------------------------------------ main ----
@@ -295,7 +398,11 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--oracle-timing", action="store_true",
-                    help="time the CPU oracle on the 256^3 and 2048^3 workloads, one thread and all cores")
+                    help="only time the CPU oracle on the 256^3 and 2048^3 workloads, one thread and all cores")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the other workloads, the oracle timing and the sustained loop after the headline")
+    ap.add_argument("--sustained-seconds", type=float, default=1.2,
+                    help="length of the sustained headline loop reported beside the K timed steps")
     ap.add_argument("--sweep", default=None, metavar="JSONL",
                     help="measure every workload of the table (and --sweep-variants, --sweep-schedules), one JSON "
                          "record per line appended to JSONL; records already there are skipped, so an "
@@ -359,15 +466,19 @@ def main():
         if s != hgemm.HGEMM_OK:
             raise hgemm.HgemmError(s, "hgemm_run")
 
-    for i in range(args.warmup):
-        step(i)
+    # One checked launch (allocates the workspace, reports any device-side
+    # error), then the clock sampler gets going; the W warm-up steps run last,
+    # right before the timed region, so that the GPU is not idle in between.
+    step(0)
     st, detail = handle.sync_status()
     if st != hgemm.HGEMM_OK:
-        raise hgemm.HgemmError(st, "warm-up (detail %s)" % hex(detail))
-
-    # ------------------------------------------------ device-timed region ----
+        raise hgemm.HgemmError(st, "first launch (detail %s)" % hex(detail))
     sampler = ClockSampler(local)
     time.sleep(0.3)
+    for i in range(args.warmup):
+        step(i)
+
+    # ------------------------------------------------ device-timed region ----
     # Two events bracket the K launches: events between launches would break the
     # overlap of consecutive kernels (programmatic dependent launch).
     t_start = torch.cuda.Event(enable_timing=True)
@@ -403,6 +514,36 @@ def main():
     torch.cuda.synchronize(dev)
     per_launch = sorted(e[0].elapsed_time(e[1]) for e in ev)
     median_ms = per_launch[len(per_launch) // 2]
+
+    # A sustained loop of the same launches, long enough (>= 1 s) for the
+    # clock sampler to see the SM clock and the power cap during it; the K
+    # timed steps above are far shorter than one sampling period.
+    sustained_rec = None
+    if world == 1 and not args.no_secondary and args.sustained_seconds > 0:
+        n_long = max(args.steps, int(math.ceil(args.sustained_seconds / (kernel_ms_avg / 1e3))))
+        s_sampler = ClockSampler(local)
+        time.sleep(0.3)
+        for i in range(args.warmup):
+            step(i)
+        l0 = torch.cuda.Event(enable_timing=True)
+        l1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        g0 = time.time()
+        l0.record(stream)
+        for i in range(n_long):
+            step(i)
+        l1.record(stream)
+        torch.cuda.synchronize(dev)
+        g1 = time.time()
+        time.sleep(0.1)
+        s_sampler.stop()
+        st, detail = handle.sync_status()
+        if st != hgemm.HGEMM_OK:
+            raise hgemm.HgemmError(st, "sustained loop (detail %s)" % hex(detail))
+        long_ms = l0.elapsed_time(l1) / n_long
+        sustained_rec = {"steps": n_long, "seconds": round(n_long * long_ms / 1e3, 3), "ms_per_step": round(long_ms, 5),
+                         "value": round(per_step / (long_ms / 1e3), 3), "unit": unit,
+                         "clocks": s_sampler.summary(g0, g1)}
 
     # ------------------------------------------------------ end to end ------
     e2e_steps = args.e2e_steps if args.e2e_steps is not None else max(3, min(args.steps, 50))
@@ -453,22 +594,14 @@ def main():
     e2e_value = world * e2e_steps * per_step / (e2e_ms / 1e3)
     peaks, peak_src = load_peaks()
     timed_seconds = total_ms / 1e3
-    if bound == "tensor":
-        # The sustained (power-capped) peak applies once the loop runs long enough
-        # for the power cap to engage, which the clock record shows.
-        sustained = timed_seconds > 1.0 or "sw_power_cap" in (clocks.get("reasons") or [])
-        peak = peaks.get("bf16_tflops_sustained" if sustained else "bf16_tflops")
-        achieved = (w.flops / 1e12) / (kernel_ms_avg / 1e3)
-        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
-                "frac": round(achieved / peak, 4), "peak_source": "%s %s" % (peak_src,
-                                                                             "sustained" if sustained else "burst")}
-    else:
-        peak = peaks.get("hbm_gbs")
-        achieved = (w.compulsory_bytes / 1e9) / (kernel_ms_avg / 1e3)
-        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "peak_source": peak_src}
+    # The sustained (power-capped) peak applies once the loop runs long enough
+    # for the power cap to engage, which the clock record shows.
+    sustained = timed_seconds > 1.0 or "sw_power_cap" in (clocks.get("reasons") or [])
+    roof = roofline_for(w, bound, kernel_ms_avg, peaks, peak_src, sustained)
     roof["traffic"] = load_traffic(w.name, plan.variant, plan)
     roof["kernel_ms_avg"] = round(kernel_ms_avg, 5)
+    if sustained_rec is not None and bound == "tensor":
+        sustained_rec["roofline"] = roofline_for(w, bound, sustained_rec["ms_per_step"], peaks, peak_src, True)
 
     cpu = None
     if not args.no_cpu_baseline and world == 1:
@@ -477,20 +610,44 @@ def main():
         cpu_val = (per_step * frac) / secs
         cpu = {"value": round(cpu_val, 6), "unit": unit, "cores": cores, "kind": "oracle",
                "sample": "first %d of %d rows of C (%.3g s, fp64 oracle, %d threads)" % (rows, w.M, secs, cores)}
+    handle.close()
 
+    # The other workloads the targets name (8192^3 bf16 and the skinny product
+    # against HBM) and the two weakest shapes, timed the same way, each with its
+    # own roofline; then the oracle on the 256^3 workload and 2048^3, one
+    # thread and all cores, on this host.
+    secondary, oracle_recs = None, None
+    if world == 1 and not args.no_secondary:
+        secondary = []
+        for name in SECONDARY:
+            sw = workloads.WORKLOADS[name]
+            s_metric, s_unit, s_per_step, s_bound = workload_metric(sw)
+            n_steps = max(args.steps, 20)
+            ms, single_ms, s_plan, _ = time_workload(sw, dev, n_steps, max(args.warmup, 5), 20)
+            r = roofline_for(sw, s_bound, ms, peaks, peak_src, False)
+            r["traffic"] = load_traffic(sw.name, s_plan.variant, s_plan)
+            secondary.append({"workload": name, "metric": s_metric, "value": round(s_per_step / (ms / 1e3), 3),
+                              "unit": s_unit, "steps": n_steps, "ms_per_step": round(ms, 5),
+                              "median_single_launch_ms": round(single_ms, 5),
+                              "value_at_median_single_launch": round(s_per_step / (single_ms / 1e3), 3),
+                              "variant": list(hgemm.VARIANTS)[s_plan.variant], "roofline": r})
+        oracle_recs = oracle_timing(emit=False)
+
+    config = problem_config(w, world)
     out = {
         "metric": metric, "value": round(value, 3), "unit": unit, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(total_ms_max / args.steps, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.in_dtype, "data": "synthetic",
-        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "layout": w.layout, "in": w.in_dtype,
-                   "acc": w.acc_dtype, "out": w.out_dtype, "variant": list(hgemm.VARIANTS)[plan.variant],
-                   "grid": plan.grid if args.schedule == "static" else plan.work_ids * plan.cta_group,
-                   "schedule": args.schedule, "epilogue": args.epilogue, "group_m": plan.group_m, "tile": [plan.tile_m, plan.tile_n], "stages": plan.stages,
-                   "stream_k": {"dp_tiles": plan.dp_tiles, "sk_units": plan.sk_units} if plan.stream_k else None,
-                   "parallelism": "replicas" if world > 1 else "single",
-                   "l2": "inputs rotate over %d copies (%.0f MiB > 2x L2)" % (copies, copies * (in_bytes + c_bytes) / 2**20),
-                   "median_single_launch_ms": round(median_ms, 5), "single_launches": n_med,
-                   "value_at_median_single_launch": round(per_step / (median_ms / 1e3), 3)},
+        "config": config,
+        "plan": {"variant": list(hgemm.VARIANTS)[plan.variant],
+                 "grid": plan.grid if args.schedule == "static" else plan.work_ids * plan.cta_group,
+                 "schedule": args.schedule, "epilogue": args.epilogue, "group_m": plan.group_m,
+                 "tile": [plan.tile_m, plan.tile_n], "stages": plan.stages,
+                 "stream_k": {"dp_tiles": plan.dp_tiles, "sk_units": plan.sk_units, "sk_ranges": plan.sk_ranges,
+                              "sk_pieces": plan.sk_pieces} if plan.stream_k else None,
+                 "input_copies": copies, "input_bytes": int(copies * (in_bytes + c_bytes))},
+        "single_launch": {"median_ms": round(median_ms, 5), "launches": n_med,
+                          "value_at_median": round(per_step / (median_ms / 1e3), 3)},
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_value, 3), "unit": unit, "h2d_bytes_per_step": int(in_bytes),
@@ -499,7 +656,12 @@ def main():
         "gpu_launches": args.steps,
         "clocks": clocks,
     }
-    handle.close()
+    if sustained_rec is not None:
+        out["sustained"] = sustained_rec
+    if secondary is not None:
+        out["secondary"] = secondary
+    if oracle_recs is not None:
+        out["oracle_timing"] = oracle_recs
     print(json.dumps(out), flush=True)
 
 
@@ -637,7 +799,7 @@ def run_reference(args, w, metric, unit, per_step, world, rank):
     out = {"impl": "reference", "metric": metric, "value": round(value, 6), "unit": unit, "n_gpus": world,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * total / args.steps, 3),
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-           "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "layout": w.layout, "in": w.in_dtype},
+           "config": problem_config(w, world),
            "cpu_baseline": {"value": round(value, 6), "unit": unit, "cores": cores, "kind": "oracle",
                             "sample": sample},
            "e2e": {"value": round(value, 6), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
