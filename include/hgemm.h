@@ -91,15 +91,11 @@ typedef enum {
                                   kernels append to (0 = off, the default); hgemm_trace_read */
   HGEMM_OPT_SCHEDULE = 8,      /* value: an hgemm_schedule_t for the dense kernels           */
   HGEMM_OPT_EPILOGUE = 9,      /* value: an hgemm_epilogue_t for the dense kernels           */
-  HGEMM_OPT_CHECKS = 10,       /* value: 1 = the kernels check their invariants (work ids from
+  HGEMM_OPT_CHECKS = 10        /* value: 1 = the kernels check their invariants (work ids from
                                   launch control in range, work items and tiles in range,
                                   fix-up tickets not past the contributor count, partial
                                   slots in range) and report a violation as HGEMM_ERR_CHECK
                                   instead of trapping; 0 (default) = no checks              */
-  HGEMM_OPT_PDL_PREFETCH = 12  /* value: 0..64; dense kernels: before waiting for the
-                                  previous kernel in the stream, the producer prefetches into
-                                  L2 this many k-blocks of its first work item (0 = none,
-                                  the default)                                               */
 } hgemm_option_t;
 
 /* Check numbers reported with HGEMM_ERR_CHECK (detail bits 8-15). */

@@ -50,7 +50,6 @@ struct Ctx {
   int stream_k = 1;  // 0 never, 1 when the estimate says so, 2 whenever the tile count leaves a partial wave
   int schedule = HGEMM_SCHEDULE_STATIC;
   int epilogue = HGEMM_EPILOGUE_TMA_STORE;
-  int pdl_prefetch = 0;  // dense: k-blocks of the first item prefetched before the wait on the previous grid
   bool checks = false;
   TraceBuf* trace = nullptr;  // device trace buffer (HGEMM_OPT_TRACE)
   int64_t trace_capacity = 0;
@@ -619,10 +618,6 @@ hgemm_status_t hgemm_set_option(hgemm_handle_t h, int32_t option, int64_t value)
       if (value != HGEMM_EPILOGUE_TMA_STORE && value != HGEMM_EPILOGUE_DIRECT) return HGEMM_ERR_INVALID_ARG;
       h->epilogue = (int)value;
       return HGEMM_OK;
-    case HGEMM_OPT_PDL_PREFETCH:
-      if (value < 0 || value > 64) return HGEMM_ERR_INVALID_ARG;
-      h->pdl_prefetch = (int)value;
-      return HGEMM_OK;
     case HGEMM_OPT_TRACE: {
       if (value < 0 || value > (int64_t)1 << 26) return HGEMM_ERR_INVALID_ARG;
       if (h->trace) {
@@ -737,7 +732,6 @@ hgemm_status_t hgemm_run(hgemm_handle_t h, const void* A, const void* B, void* C
   args.acc_f16 = acc_dtype == HGEMM_F16;
   args.out_bf16 = out_dtype == HGEMM_BF16;
   args.inject = h->inject;
-  args.pdl_prefetch = h->pdl_prefetch;
   args.timeout_ns = h->timeout_ns;
   args.status = h->status;
   args.trace = h->trace;

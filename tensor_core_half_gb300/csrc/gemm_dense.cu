@@ -183,23 +183,6 @@ __global__ void __launch_bounds__(192, 1)
   const WaitCtl ctl{args.timeout_ns, abort_flag};
   const WaitCtl drain_ctl{kDrainTimeoutNs, nullptr};
 
-  // L2 prefetch of the boxes that the load of k-block kb of tile tc will read
-  // (the same coordinates as the loads below).  Only used before the wait on
-  // the previous grid: inside the mainloop every prefetch costs the issuing
-  // SM's TMA unit about as much as a load (measured: one prefetch per load
-  // made 4096^3 40 % slower), and the loads are what limit the mainloop.
-  auto prefetch_kb = [&](const TileCoord& tc, int kb) {
-    const int k0 = kb * S::BK;
-    tma_prefetch_2d(&tmA, k0, tc.m * (S::BM * CG) + (int)rank * S::BM);
-    const int n_row = tc.n * BN + (int)rank * S::B_ROWS;
-    if (!args.b_mn_major) {
-      tma_prefetch_2d(&tmB, k0, n_row);
-    } else if constexpr (S::kMNMajorOK) {
-#pragma unroll
-      for (int j = 0; j < S::B_ROWS / 64; ++j) tma_prefetch_2d(&tmB, n_row + 64 * j, k0);
-    }
-  };
-
   // ------------------------------------------------------------ setup ----
   if (warp == 0) {
     if (lane == 0) {
@@ -237,20 +220,6 @@ __global__ void __launch_bounds__(192, 1)
   // The prologue above touched no global memory; from here on the previous
   // kernel in the stream (launched with programmatic serialisation) must be done.
   pdl_launch_dependents();
-  if (warp == 0 && lane == 0 && args.pdl_prefetch > 0) {
-    // While the previous grid finishes, bring the first k-blocks of this
-    // cluster's first item into L2 (both schedules start with id = cluster).
-    // A prefetch only reads global memory into L2, the point of coherence, so
-    // it cannot return stale data whatever the previous grid writes.
-    WorkIter it0(args.sk_ranges, args.dp_tiles, args.sk_units, args.k_blocks);
-    it0.start_static(cluster, nclusters);
-    WorkItem w0;
-    if (it0.next_static(w0)) {
-      const TileCoord tc0 = tile_coord(w0.tile, args.tiles_m, args.tiles_n, args.group_m);
-      const int end = min(w0.kb1, w0.kb0 + args.pdl_prefetch);
-      for (int kb = w0.kb0; kb < end; ++kb) prefetch_kb(tc0, kb);
-    }
-  }
   pdl_wait_prior_grid();
   TraceBuf* const tb = args.trace;
   if (threadIdx.x == 0) trace_event(tb, 0, kTraceKernelBegin, -1, (int32_t)(clock64() & 0x7fffffff));

@@ -64,7 +64,6 @@ struct DenseArgs {
   int32_t acc_f16;         // fp16 accumulators in tensor memory (one per 32-bit column, low half)
   int32_t out_bf16;        // output dtype: 1 bf16, 0 fp16
   int32_t inject;          // test-only fault injection (HGEMM_OPT_INJECT_FAULT)
-  int32_t pdl_prefetch;    // k-blocks of the first work item prefetched into L2 before the wait on the previous grid
   uint64_t timeout_ns;
   int32_t* status;
   TraceBuf* trace;         // null unless tracing
