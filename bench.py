@@ -289,6 +289,27 @@ def oracle_timing(names=("square256_f16", "sweep2048_f16_accf32"), emit=True):
     return out
 
 
+def wake_then_rest(step, dev, load_seconds, rest_seconds):
+    """Brings a GPU that has been idle out of its low-clock state: launches
+    back to back for load_seconds, then lets it rest for rest_seconds so that
+    the power limiter, which engages within tens of milliseconds of full load,
+    has recovered when the timed burst starts.  (Measured on GB300 at 4096^3:
+    the first bursts of a process on an idle GPU ran ~81 us per launch, bursts
+    during or right after 50 ms-3 s of load ~88 us, bursts after such load
+    and >= 0.5 s of rest ~77 us.)  Returns what it did."""
+    import torch
+    t0 = time.time()
+    n = 0
+    while time.time() - t0 < load_seconds:
+        for _ in range(32):
+            step(n)
+            n += 1
+        torch.cuda.synchronize(dev)
+    loaded = time.time() - t0
+    time.sleep(rest_seconds)
+    return {"load_launches": n, "load_seconds": round(loaded, 3), "rest_seconds": rest_seconds}
+
+
 def problem_config(w, world):
     """The workload as both arms name it (the same dict in our line and in the
     reference arm's line)."""
@@ -317,7 +338,9 @@ def time_workload(w, dev, steps, warmup, n_single, sampler_index=None):
     """Device-timed launches of one workload through hgemm_run: `steps`
     back-to-back launches between two events (inputs rotating over copies
     larger than 2x L2), then the median of `n_single` launches each between
-    its own events.  Returns (ms per launch, median single ms, plan, clocks)."""
+    its own events.  Before the warm-up, the same load-then-rest as the
+    headline.  Returns (ms per launch, median single ms, plan, what the
+    load-then-rest did)."""
     import torch
 
     from tensor_core_half_gb300 import hgemm, workloads
@@ -340,9 +363,9 @@ def time_workload(w, dev, steps, warmup, n_single, sampler_index=None):
             if s != hgemm.HGEMM_OK:
                 raise hgemm.HgemmError(s, "hgemm_run (%s)" % w.name)
 
+        protocol = wake_then_rest(step, dev, 0.05, 0.6)
         for i in range(warmup):
             step(i)
-        torch.cuda.synchronize(dev)
         sampler = ClockSampler(sampler_index) if sampler_index is not None else None
         if sampler:
             time.sleep(0.25)
@@ -373,7 +396,7 @@ def time_workload(w, dev, steps, warmup, n_single, sampler_index=None):
             raise hgemm.HgemmError(st, "%s (detail %s)" % (w.name, hex(detail)))
     del A, B, C
     torch.cuda.empty_cache()
-    return ms, single[len(single) // 2], plan, clocks
+    return ms, single[len(single) // 2], plan, protocol
 
 
 SECONDARY = ("square8192_bf16", "skinny16x16384x8192_bf16", "ragged1000x3000x4104_bf16", "sweep2048_f16_accf32")
@@ -401,6 +424,10 @@ def main():
                     help="only time the CPU oracle on the 256^3 and 2048^3 workloads, one thread and all cores")
     ap.add_argument("--no-secondary", action="store_true",
                     help="skip the other workloads, the oracle timing and the sustained loop after the headline")
+    ap.add_argument("--wake-seconds", type=float, default=0.3,
+                    help="untimed back-to-back launches that bring an idle GPU to its full clock before the rest")
+    ap.add_argument("--rest-seconds", type=float, default=0.6,
+                    help="idle time after the wake-up load, before the W warm-up steps and the timed region")
     ap.add_argument("--sustained-seconds", type=float, default=1.2,
                     help="length of the sustained headline loop reported beside the K timed steps")
     ap.add_argument("--sweep", default=None, metavar="JSONL",
@@ -474,7 +501,9 @@ def main():
     if st != hgemm.HGEMM_OK:
         raise hgemm.HgemmError(st, "first launch (detail %s)" % hex(detail))
     sampler = ClockSampler(local)
-    time.sleep(0.3)
+    # Load, then rest (see wake_then_rest), then the W warm-up steps right
+    # before the timed region.
+    clock_warm = wake_then_rest(step, dev, args.wake_seconds, max(0.3, args.rest_seconds))
     for i in range(args.warmup):
         step(i)
 
@@ -623,14 +652,15 @@ def main():
             sw = workloads.WORKLOADS[name]
             s_metric, s_unit, s_per_step, s_bound = workload_metric(sw)
             n_steps = max(args.steps, 20)
-            ms, single_ms, s_plan, _ = time_workload(sw, dev, n_steps, max(args.warmup, 5), 20)
+            ms, single_ms, s_plan, s_protocol = time_workload(sw, dev, n_steps, max(args.warmup, 5), 20)
             r = roofline_for(sw, s_bound, ms, peaks, peak_src, False)
             r["traffic"] = load_traffic(sw.name, s_plan.variant, s_plan)
             secondary.append({"workload": name, "metric": s_metric, "value": round(s_per_step / (ms / 1e3), 3),
                               "unit": s_unit, "steps": n_steps, "ms_per_step": round(ms, 5),
                               "median_single_launch_ms": round(single_ms, 5),
                               "value_at_median_single_launch": round(s_per_step / (single_ms / 1e3), 3),
-                              "variant": list(hgemm.VARIANTS)[s_plan.variant], "roofline": r})
+                              "variant": list(hgemm.VARIANTS)[s_plan.variant], "warmup_protocol": s_protocol,
+                              "roofline": r})
         oracle_recs = oracle_timing(emit=False)
 
     config = problem_config(w, world)
@@ -646,6 +676,7 @@ def main():
                  "stream_k": {"dp_tiles": plan.dp_tiles, "sk_units": plan.sk_units, "sk_ranges": plan.sk_ranges,
                               "sk_pieces": plan.sk_pieces} if plan.stream_k else None,
                  "input_copies": copies, "input_bytes": int(copies * (in_bytes + c_bytes))},
+        "warmup_protocol": clock_warm,
         "single_launch": {"median_ms": round(median_ms, 5), "launches": n_med,
                           "value_at_median": round(per_step / (median_ms / 1e3), 3)},
         "roofline": roof,
