@@ -491,7 +491,9 @@ CHECKED_CASES = [("2sm256", "TN", 4096, 4096, 256, 2, "static"), ("2sm256", "TN"
                  ("1sm128", "NN", 1000, 3000, 520, 1, "dynamic"), ("2sm192", "TN", 1000, 3000, 4104, 1, "static"),
                  ("1sm256", "TN", 2048, 4096, 192, 1, "dynamic"), ("2sm256", "NN", 768, 520, 4104, 1, "static"),
                  ("splitk", "TN", 16, 16384, 4096, 1, "static"), ("splitk", "TN", 16, 16384, 4096, 2, "static"),
-                 ("splitk", "TN", 40, 8192, 8192, 1, "dynamic")]
+                 ("splitk", "TN", 40, 8192, 8192, 1, "dynamic"),
+                 ("2sm256", "TN", 4096, 4096, 1024, 3, "static"), ("2sm256", "NN", 4096, 4096, 1024, 3, "dynamic"),
+                 ("1sm128", "TN", 1000, 3000, 520, 3, "static")]
 
 
 @pytest.mark.parametrize("variant,layout,M,N,K,sk,schedule", CHECKED_CASES)
@@ -505,11 +507,12 @@ def test_checked_runs_report_nothing(h, variant, layout, M, N, K, sk, schedule):
     parity.check(got, ab, bb, M, N, K, layout, "bf16", "f32", "bf16")
 
 
+@pytest.mark.parametrize("sk", [2, 3], ids=["ranges", "pieces"])
 @pytest.mark.parametrize("variant,M,N,K,schedule", [("2sm256", 4096, 4096, 256, "static"),
                                                     ("2sm256", 4096, 4096, 256, "dynamic"),
                                                     ("splitk", 16, 16384, 4096, "static"),
                                                     ("splitk", 16, 16384, 4096, "dynamic")])
-def test_checks_catch_corrupted_tickets(h, variant, M, N, K, schedule):
+def test_checks_catch_corrupted_tickets(h, variant, M, N, K, schedule, sk):
     # The host fills the fix-up ticket counters with 0x01 bytes before the
     # launch: every ticket is then far past its tile's contributor count.  The
     # kernels only compare tickets (no access depends on them, no wait), so the
@@ -519,7 +522,7 @@ def test_checks_catch_corrupted_tickets(h, variant, M, N, K, schedule):
     C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
     h.set_option(hgemm.HGEMM_OPT_FORCE_VARIANT, hgemm.VARIANTS[variant])
     h.set_option(hgemm.HGEMM_OPT_SCHEDULE, hgemm.SCHEDULES[schedule])
-    h.set_option(hgemm.HGEMM_OPT_STREAM_K, 2)  # split the dense tiles even where the estimate would not
+    h.set_option(hgemm.HGEMM_OPT_STREAM_K, sk)  # split the dense tiles even where the estimate would not
     h.set_option(hgemm.HGEMM_OPT_CHECKS, 1)
     h.set_option(hgemm.HGEMM_OPT_INJECT_FAULT, 2)
     try:
