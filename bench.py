@@ -296,7 +296,9 @@ def wake_then_rest(step, dev, load_seconds, rest_seconds):
     has recovered when the timed burst starts.  (Measured on GB300 at 4096^3:
     the first bursts of a process on an idle GPU ran ~81 us per launch, bursts
     during or right after 50 ms-3 s of load ~88 us, bursts after such load
-    and >= 0.5 s of rest ~77 us.)  Returns what it did."""
+    and >= 0.5 s of rest ~77 us.  As the first process on a fresh box, 1 s of
+    load and 1 s of rest gave 77.6 us where 0.3 s and 0.6 s had given
+    79-80 us on other boxes.)  Returns what it did."""
     import torch
     t0 = time.time()
     n = 0
@@ -424,9 +426,9 @@ def main():
                     help="only time the CPU oracle on the 256^3 and 2048^3 workloads, one thread and all cores")
     ap.add_argument("--no-secondary", action="store_true",
                     help="skip the other workloads, the oracle timing and the sustained loop after the headline")
-    ap.add_argument("--wake-seconds", type=float, default=0.3,
+    ap.add_argument("--wake-seconds", type=float, default=1.0,
                     help="untimed back-to-back launches that bring an idle GPU to its full clock before the rest")
-    ap.add_argument("--rest-seconds", type=float, default=0.6,
+    ap.add_argument("--rest-seconds", type=float, default=1.0,
                     help="idle time after the wake-up load, before the W warm-up steps and the timed region")
     ap.add_argument("--sustained-seconds", type=float, default=1.2,
                     help="length of the sustained headline loop reported beside the K timed steps")
