@@ -111,6 +111,36 @@ def test_reference_arm_prints_the_contract_line():
     assert d["metric"].startswith("TFLOPS") and d["unit"] == "TFLOPS" and d["higher_is_better"] is True
     assert d["value"] > 0 and d["ms_per_step"] > 0 and d["vs_baseline"] is None
     assert d["data"] == "synthetic" and d["config"]["workload"] == "square4096_bf16"
+    # the same problem config the CUDA arm prints (sizes, layout and all three dtypes)
+    from tensor_core_half_gb300 import workloads
+    assert d["config"] == bench.problem_config(workloads.WORKLOADS["square4096_bf16"], 1)
+    assert (d["config"]["in"], d["config"]["acc"], d["config"]["out"]) == ("bf16", "f32", "bf16")
     cpu = d["cpu_baseline"]
     assert cpu["kind"] == "oracle" and cpu["cores"] >= 1 and cpu["value"] == d["value"] and cpu["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_roofline_object_uses_the_peak_of_its_bound():
+    from tensor_core_half_gb300 import workloads
+    peaks = {"hbm_gbs": 6000.0, "bf16_tflops": 2000.0, "bf16_tflops_sustained": 1600.0}
+    w = workloads.WORKLOADS["square4096_bf16"]
+    ms = 0.08
+    r = bench.roofline_for(w, "tensor", ms, peaks, "measured", False)
+    assert r["bound"] == "tensor" and r["peak"] == 2000.0 and r["unit"] == "TFLOP/s"
+    assert math.isclose(r["achieved"], round(w.flops / 1e12 / (ms / 1e3), 2))
+    assert math.isclose(r["frac"], round(r["achieved"] / 2000.0, 4), abs_tol=1e-4)
+    assert bench.roofline_for(w, "tensor", ms, peaks, "measured", True)["peak"] == 1600.0
+    s = workloads.WORKLOADS["skinny16x16384x8192_bf16"]
+    r = bench.roofline_for(s, "hbm", 0.045, peaks, "measured", False)
+    assert r["bound"] == "hbm" and r["peak"] == 6000.0 and r["unit"] == "GB/s"
+    assert math.isclose(r["achieved"], round(s.compulsory_bytes / 1e9 / 45e-6, 1))
+
+
+def test_secondary_workloads_cover_the_targets():
+    # 8192^3 bf16 and the skinny product are targets of their own; the other
+    # two are the shapes with less than one wave of tiles
+    from tensor_core_half_gb300 import workloads
+    assert set(bench.SECONDARY) <= set(workloads.WORKLOADS)
+    assert "square8192_bf16" in bench.SECONDARY and "skinny16x16384x8192_bf16" in bench.SECONDARY
+    assert bench.workload_metric(workloads.WORKLOADS["skinny16x16384x8192_bf16"])[3] == "hbm"
+    assert bench.workload_metric(workloads.WORKLOADS["square8192_bf16"])[3] == "tensor"
