@@ -277,7 +277,7 @@ typedef struct {
   int64_t workspace_bytes; /* split-K / stream-K partial sums + tickets                  */
   int32_t dp_tiles;      /* dense: tiles computed whole, dealt round-robin (all if no stream-K) */
   int32_t stream_k;      /* dense: 1 when the remaining tiles are split along K            */
-  int64_t sk_units;      /* dense: (num_tiles - dp_tiles) * k_blocks, cut evenly over clusters */
+  int64_t sk_units;      /* dense: (num_tiles - dp_tiles) * k_blocks, cut evenly into sk_ranges ranges */
   int32_t sk_ranges;     /* dense: stream-K ranges, work ids [0, sk_ranges); 0 without stream-K */
   int32_t work_ids;      /* dense: sk_ranges + dp_tiles; ids >= sk_ranges are whole tiles  */
   int32_t schedule;      /* hgemm_schedule_t the plan was made for                         */
