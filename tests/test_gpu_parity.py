@@ -324,6 +324,24 @@ def test_stream_k_pieces_at_wave_scale(h, M, N, K):
         assert np.array_equal(got, run(h, a, b, M, N, K, "TN", "f32", "bf16", stream_k=sk))
 
 
+@pytest.mark.parametrize("M,N,K,layout,combo", [(4096, 4096, 1032, "NN", ("f16", "f16", "f16")),
+                                                 (4096, 5120, 1080, "TN", ("bf16", "f32", "bf16")),
+                                                 (2560, 9984, 776, "NN", ("bf16", "f32", "f16"))])
+def test_stream_k_pieces_odd_k_blocks(h, M, N, K, layout, combo):
+    """K pieces forced (stream-K 3) where the k-block count is odd, so a
+    tile's pieces differ by one k-block, on NN and fp16-accumulate plans at
+    wave scale: sampled parity and run-to-run identity."""
+    fin, acc, out = combo
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    st, p = hgemm.hgemm_plan(M, N, K, hgemm.LAYOUTS[layout], hgemm.DTYPES[fin], hgemm.DTYPES[acc], hgemm.DTYPES[out],
+                             sms, hgemm.HGEMM_VARIANT_AUTO, 0, 3)
+    assert st == 0 and p.stream_k and p.sk_pieces >= 2 and p.dp_tiles > 0 and p.k_blocks % 2 == 1
+    a, b, ab, bb = parity.inputs(M, N, K, layout, fin, ("uniform", -1.0, 1.0), 64)
+    got = run(h, a, b, M, N, K, layout, acc, out, stream_k=3)
+    parity.check(got, ab, bb, M, N, K, layout, fin, acc, out, sampled=True)
+    assert np.array_equal(got, run(h, a, b, M, N, K, layout, acc, out, stream_k=3))
+
+
 # Dynamic schedule (cluster launch control).  Shapes with more work ids than
 # resident clusters, so that running clusters cancel pending ones and take
 # their ids, with and without stream-K ranges; plus a ragged shape.
