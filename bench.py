@@ -169,6 +169,21 @@ class ClockSampler:
                 "power_w_max": max(pw) if pw else None, "samples": len(inside), "window": window}
 
 
+def in_kernel_clocks(rows, recorded, expected):
+    """SM clock of every CTA of the timed launches from their kernel begin/end
+    stamps (cycles over global-timer ns), as median / min / max MHz."""
+    from tensor_core_half_gb300 import trace
+
+    mhz = sorted(trace.launch_clocks(rows))
+    out = {"source": "SM cycle counter / global timer between each CTA's kernel begin and end, every CTA of "
+                     "the K timed launches",
+           "stamps": int(recorded), "stamps_expected": int(expected), "cta_launches": len(mhz)}
+    if mhz:
+        out.update({"sm_mhz_median": round(mhz[len(mhz) // 2], 1), "sm_mhz_min": round(mhz[0], 1),
+                    "sm_mhz_max": round(mhz[-1], 1)})
+    return out
+
+
 # --------------------------------------------------------------- helpers ----
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -336,13 +351,16 @@ def roofline_for(w, bound, kernel_ms, peaks, peak_src, sustained):
             "frac": round(achieved / peak, 4), "peak_source": peak_src}
 
 
-def time_workload(w, dev, steps, warmup, n_single, sampler_index=None):
+def time_workload(w, dev, steps, warmup, n_single, stamps=True):
     """Device-timed launches of one workload through hgemm_run: `steps`
     back-to-back launches between two events (inputs rotating over copies
     larger than 2x L2), then the median of `n_single` launches each between
     its own events.  Before the warm-up, the same load-then-rest as the
-    headline.  Returns (ms per launch, median single ms, plan, what the
-    load-then-rest did)."""
+    headline.  With `stamps`, every CTA records its kernel begin and end
+    (HGEMM_OPT_TRACE_ITEMS = 0) from the first launch on, and those of the
+    timed launches give the SM clock inside them.  Returns (ms per launch,
+    median single ms, plan, what the load-then-rest did, in-kernel clocks or
+    None)."""
     import torch
 
     from tensor_core_half_gb300 import hgemm, workloads
@@ -358,7 +376,13 @@ def time_workload(w, dev, steps, warmup, n_single, sampler_index=None):
     st, plan = hgemm.hgemm_plan(w.M, w.N, w.K, lay, fin, facc, fout,
                                 torch.cuda.get_device_properties(dev).multi_processor_count)
     stream = torch.cuda.current_stream(dev)
+    capacity = 2 * plan.grid * (steps + 2)
+    clocks = None
     with hgemm.Handle() as h:
+        if stamps:
+            h.set_option(hgemm.HGEMM_OPT_TRACE, capacity)
+            h.set_option(hgemm.HGEMM_OPT_TRACE_ITEMS, 0)
+
         def step(i):
             s = hgemm.hgemm_run(h.h, A[i % copies].data_ptr(), B[i % copies].data_ptr(), C[i % copies].data_ptr(),
                                 w.M, w.N, w.K, lay, fin, facc, fout, stream.cuda_stream)
@@ -368,24 +392,25 @@ def time_workload(w, dev, steps, warmup, n_single, sampler_index=None):
         protocol = wake_then_rest(step, dev, 0.05, 0.6)
         for i in range(warmup):
             step(i)
-        sampler = ClockSampler(sampler_index) if sampler_index is not None else None
-        if sampler:
-            time.sleep(0.25)
+        if stamps:  # drop the warm-up's stamps
+            st = hgemm.hgemm_trace_read(h.h, 0)[0]
+            if st != hgemm.HGEMM_OK:
+                raise hgemm.HgemmError(st, "hgemm_trace_read (reset, %s)" % w.name)
+        torch.cuda.synchronize(dev)
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
-        h0 = time.time()
         e0.record(stream)
         for i in range(steps):
             step(i)
         e1.record(stream)
         torch.cuda.synchronize(dev)
-        h1 = time.time()
-        clocks = None
-        if sampler:
-            time.sleep(0.1)
-            sampler.stop()
-            clocks = sampler.summary(h0, h1)
         ms = e0.elapsed_time(e1) / steps
+        if stamps:
+            st, recorded, rows = hgemm.hgemm_trace_read(h.h, capacity)
+            if st != hgemm.HGEMM_OK:
+                raise hgemm.HgemmError(st, "hgemm_trace_read (%s)" % w.name)
+            h.set_option(hgemm.HGEMM_OPT_TRACE, 0)
+            clocks = in_kernel_clocks(rows, recorded, 2 * plan.grid * steps)
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_single)]
         for i, (x, y) in enumerate(ev):
             x.record(stream)
@@ -398,7 +423,7 @@ def time_workload(w, dev, steps, warmup, n_single, sampler_index=None):
             raise hgemm.HgemmError(st, "%s (detail %s)" % (w.name, hex(detail)))
     del A, B, C
     torch.cuda.empty_cache()
-    return ms, single[len(single) // 2], plan, protocol
+    return ms, single[len(single) // 2], plan, protocol, clocks
 
 
 SECONDARY = ("square8192_bf16", "skinny16x16384x8192_bf16", "ragged1000x3000x4104_bf16", "sweep2048_f16_accf32")
@@ -432,6 +457,9 @@ def main():
                     help="idle time after the wake-up load, before the W warm-up steps and the timed region")
     ap.add_argument("--sustained-seconds", type=float, default=1.2,
                     help="length of the sustained headline loop reported beside the K timed steps")
+    ap.add_argument("--no-launch-clocks", action="store_true",
+                    help="do not record each CTA's kernel begin/end stamps (SM cycle counter and global timer) "
+                         "during the headline, which give the SM clock inside the K timed launches")
     ap.add_argument("--sweep", default=None, metavar="JSONL",
                     help="measure every workload of the table (and --sweep-variants, --sweep-schedules), one JSON "
                          "record per line appended to JSONL; records already there are skipped, so an "
@@ -495,6 +523,17 @@ def main():
         if s != hgemm.HGEMM_OK:
             raise hgemm.HgemmError(s, "hgemm_run")
 
+    # The SM clock inside the timed region: nvidia-smi samples every 20 ms,
+    # far apart for K launches of well under a millisecond, so every CTA of
+    # every launch also records its kernel begin and end (the SM cycle
+    # counter against the global timer; two appends per CTA, from the first
+    # launch on, so the warm-up runs the same code as the timed launches).
+    launch_clocks = world == 1 and not args.no_launch_clocks
+    stamp_capacity = 2 * plan.grid * (args.steps + 2)
+    if launch_clocks:
+        handle.set_option(hgemm.HGEMM_OPT_TRACE, stamp_capacity)
+        handle.set_option(hgemm.HGEMM_OPT_TRACE_ITEMS, 0)
+
     # One checked launch (allocates the workspace, reports any device-side
     # error), then the clock sampler gets going; the W warm-up steps run last,
     # right before the timed region, so that the GPU is not idle in between.
@@ -514,6 +553,10 @@ def main():
     # overlap of consecutive kernels (programmatic dependent launch).
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
+    if launch_clocks:  # drop the warm-up's stamps (this read synchronises the device)
+        st = hgemm.hgemm_trace_read(handle.h, 0)[0]
+        if st != hgemm.HGEMM_OK:
+            raise hgemm.HgemmError(st, "hgemm_trace_read (reset)")
     barrier(world)
     torch.cuda.synchronize(dev)
     h0 = time.time()
@@ -533,6 +576,12 @@ def main():
     time.sleep(0.2)
     sampler.stop()
     clocks = sampler.summary(h0, h1)
+    if launch_clocks:
+        st, n_stamps, rows = hgemm.hgemm_trace_read(handle.h, stamp_capacity)
+        if st != hgemm.HGEMM_OK:
+            raise hgemm.HgemmError(st, "hgemm_trace_read")
+        handle.set_option(hgemm.HGEMM_OPT_TRACE, 0)
+        clocks["in_kernel"] = in_kernel_clocks(rows, n_stamps, 2 * plan.grid * args.steps)
 
     # Median of single launches, each bracketed by its own events (outside the
     # timed region; includes the launch overhead the overlap otherwise hides).
@@ -654,7 +703,8 @@ def main():
             sw = workloads.WORKLOADS[name]
             s_metric, s_unit, s_per_step, s_bound = workload_metric(sw)
             n_steps = max(args.steps, 20)
-            ms, single_ms, s_plan, s_protocol = time_workload(sw, dev, n_steps, max(args.warmup, 5), 20)
+            ms, single_ms, s_plan, s_protocol, s_clocks = time_workload(sw, dev, n_steps, max(args.warmup, 5), 20,
+                                                                        not args.no_launch_clocks)
             r = roofline_for(sw, s_bound, ms, peaks, peak_src, False)
             r["traffic"] = load_traffic(sw.name, s_plan.variant, s_plan)
             secondary.append({"workload": name, "metric": s_metric, "value": round(s_per_step / (ms / 1e3), 3),
@@ -662,7 +712,7 @@ def main():
                               "median_single_launch_ms": round(single_ms, 5),
                               "value_at_median_single_launch": round(s_per_step / (single_ms / 1e3), 3),
                               "variant": list(hgemm.VARIANTS)[s_plan.variant], "warmup_protocol": s_protocol,
-                              "roofline": r})
+                              "clocks": {"in_kernel": s_clocks}, "roofline": r})
         oracle_recs = oracle_timing(emit=False)
 
     config = problem_config(w, world)

@@ -91,11 +91,16 @@ typedef enum {
                                   kernels append to (0 = off, the default); hgemm_trace_read */
   HGEMM_OPT_SCHEDULE = 8,      /* value: an hgemm_schedule_t for the dense kernels           */
   HGEMM_OPT_EPILOGUE = 9,      /* value: an hgemm_epilogue_t for the dense kernels           */
-  HGEMM_OPT_CHECKS = 10        /* value: 1 = the kernels check their invariants (work ids from
+  HGEMM_OPT_CHECKS = 10,       /* value: 1 = the kernels check their invariants (work ids from
                                   launch control in range, work items and tiles in range,
                                   fix-up tickets not past the contributor count, partial
                                   slots in range) and report a violation as HGEMM_ERR_CHECK
                                   instead of trapping; 0 (default) = no checks              */
+  HGEMM_OPT_TRACE_ITEMS = 11   /* value: 1 (default) = the trace (HGEMM_OPT_TRACE) records every
+                                  event kind; 0 = only each CTA's kernel begin and end records
+                                  (two per CTA per launch: the SM cycle counter against the
+                                  global timer, i.e. the SM clock during each launch, at the
+                                  cost of two appends per CTA)                               */
 } hgemm_option_t;
 
 /* Check numbers reported with HGEMM_ERR_CHECK (detail bits 8-15). */

@@ -53,6 +53,7 @@ struct Ctx {
   bool checks = false;
   TraceBuf* trace = nullptr;  // device trace buffer (HGEMM_OPT_TRACE)
   int64_t trace_capacity = 0;
+  bool trace_items = true;  // HGEMM_OPT_TRACE_ITEMS: false keeps only the kernel begin/end records
   // hgemm_run_host: two staging sets (double buffering across calls), three
   // internal streams and the events that chain them.
   struct HostStage {
@@ -626,6 +627,10 @@ hgemm_status_t hgemm_set_option(hgemm_handle_t h, int32_t option, int64_t value)
       if (value < 0 || value > 1) return HGEMM_ERR_INVALID_ARG;
       h->checks = value != 0;
       return HGEMM_OK;
+    case HGEMM_OPT_TRACE_ITEMS:
+      if (value < 0 || value > 1) return HGEMM_ERR_INVALID_ARG;
+      h->trace_items = value != 0;
+      return HGEMM_OK;
     case HGEMM_OPT_EPILOGUE:
       if (value != HGEMM_EPILOGUE_TMA_STORE && value != HGEMM_EPILOGUE_DIRECT) return HGEMM_ERR_INVALID_ARG;
       h->epilogue = (int)value;
@@ -715,6 +720,7 @@ hgemm_status_t hgemm_run(hgemm_handle_t h, const void* A, const void* B, void* C
     args.ticket_stride = kSplitKTicketStride;
     args.C = C;
     args.trace = h->trace;
+    args.trace_items = h->trace_items ? 1 : 0;
     // Dynamic schedule: one CTA per chunk; the CTAs that run take over the rest.
     return cuda_status(splitk_launch(tmW, tmX, args, args.dynamic ? p.splitk_chunks : p.grid, p.smem_bytes, s));
   }
@@ -747,6 +753,7 @@ hgemm_status_t hgemm_run(hgemm_handle_t h, const void* A, const void* B, void* C
   args.timeout_ns = h->timeout_ns;
   args.status = h->status;
   args.trace = h->trace;
+  args.trace_items = h->trace_items ? 1 : 0;
   args.dp_tiles = p.dp_tiles;
   args.sk_ranges = p.sk_ranges;
   args.sk_units = p.sk_units;

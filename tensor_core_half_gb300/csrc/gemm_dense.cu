@@ -222,7 +222,18 @@ __global__ void __launch_bounds__(192, 1)
   pdl_launch_dependents();
   pdl_wait_prior_grid();
   TraceBuf* const tb = args.trace;
-  if (threadIdx.x == 0) trace_event(tb, 0, kTraceKernelBegin, -1, (int32_t)(clock64() & 0x7fffffff));
+  TraceBuf* const tbi = args.trace_items ? tb : nullptr;  // work-item events (else only begin/end)
+  // This CTA's kernel begin and end records (with the SM cycle counter): both
+  // slots are reserved here by an epilogue thread, idle until the first
+  // accumulator is ready, so that neither the producer's first copy nor the
+  // CTA's exit waits for the trace's atomic.
+  unsigned long long stamp_slot = 0;
+  if (tb != nullptr && threadIdx.x == kStampThread) {
+    const uint64_t t = globaltimer_ns();
+    const int32_t clk = (int32_t)(clock64() & 0x7fffffff);
+    stamp_slot = trace_reserve(tb, 2ull);
+    trace_put(tb, stamp_slot, t, 0, kTraceKernelBegin, -1, clk);
+  }
 
   if (warp == 0) {
     // ------------------------------------------------- TMA producer ----
@@ -238,7 +249,7 @@ __global__ void __launch_bounds__(192, 1)
         const int got = feed.next(w, ctl);
         if (got < 0) ok = false;
         if (got <= 0) break;
-        trace_event(tb, kRoleProducer, kTraceItemBegin, w.tile, w.kb0);
+        trace_event(tbi, kRoleProducer, kTraceItemBegin, w.tile, w.kb0);
         uint32_t stall = 0;
         const TileCoord tc = tile_coord(w.tile, args.tiles_m, args.tiles_n, args.group_m);
         if (args.checks) {
@@ -301,8 +312,8 @@ __global__ void __launch_bounds__(192, 1)
             break;
           }
         }
-        trace_event(tb, kRoleProducer, kTraceStall, w.tile, (int32_t)stall);
-        trace_event(tb, kRoleProducer, kTraceItemEnd, w.tile, w.kb1);
+        trace_event(tbi, kRoleProducer, kTraceStall, w.tile, (int32_t)stall);
+        trace_event(tbi, kRoleProducer, kTraceItemEnd, w.tile, w.kb1);
         if (!ok) break;
       }
       if (!ok) {
@@ -352,7 +363,7 @@ __global__ void __launch_bounds__(192, 1)
           break;
         }
         tc_fence_after();
-        trace_event(tb, kRoleMma, kTraceItemBegin, w.tile, w.kb0);
+        trace_event(tbi, kRoleMma, kTraceItemBegin, w.tile, w.kb0);
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
         uint32_t stall = 0;
         for (int kb = w.kb0; kb < w.kb1; ++kb) {
@@ -378,8 +389,8 @@ __global__ void __launch_bounds__(192, 1)
         }
         if (!ok) break;
         tc_commit_cg<CG>(tfull_bar(acc), (uint16_t)0x3);  // accumulator ready for the epilogue
-        trace_event(tb, kRoleMma, kTraceStall, w.tile, (int32_t)stall);
-        trace_event(tb, kRoleMma, kTraceItemEnd, w.tile, w.kb1);
+        trace_event(tbi, kRoleMma, kTraceStall, w.tile, (int32_t)stall);
+        trace_event(tbi, kRoleMma, kTraceItemEnd, w.tile, w.kb1);
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
       }
@@ -508,7 +519,7 @@ __global__ void __launch_bounds__(192, 1)
       }
       tc_fence_after();
       const bool tracer = threadIdx.x == 64;
-      if (tracer) trace_event(tb, kRoleEpilogue, kTraceItemBegin, w.tile, w.slot);
+      if (tracer) trace_event(tbi, kRoleEpilogue, kTraceItemBegin, w.tile, w.slot);
       const TileCoord tc = tile_coord(w.tile, args.tiles_m, args.tiles_n, args.group_m);
       const int m0 = tc.m * (S::BM * CG) + (int)rank * S::BM + q * 32;  // first C row of this warp
       const int n0 = tc.n * BN;
@@ -562,7 +573,7 @@ __global__ void __launch_bounds__(192, 1)
           }
           named_bar_sync(1, 128);  // every row of the partial is written ...
           if (threadIdx.x == 64) red_add_release_gpu(pubs, 1);  // ... before it is published
-          if (tracer) trace_event(tb, kRoleEpilogue, kTracePartialStored, w.tile, ticket);
+          if (tracer) trace_event(tbi, kRoleEpilogue, kTracePartialStored, w.tile, ticket);
         } else {
           if (threadIdx.x == 64) {
             const bool all_in = wait_counter_geq(pubs, others, ctl);
@@ -601,7 +612,7 @@ __global__ void __launch_bounds__(192, 1)
             }
             emit_chunk(f, m0, n0 + c * 64);
           }
-          if (tracer) trace_event(tb, kRoleEpilogue, kTraceReduced, w.tile, others + 1);
+          if (tracer) trace_event(tbi, kRoleEpilogue, kTraceReduced, w.tile, others + 1);
           if (threadIdx.x == 64) {  // ready for the next launch
             *arrivals = 0;
             *pubs = 0;
@@ -609,7 +620,7 @@ __global__ void __launch_bounds__(192, 1)
         }
         named_bar_sync(1, 128);  // ticket_slot is reused by the next item
       }
-      if (tracer) trace_event(tb, kRoleEpilogue, kTraceItemEnd, w.tile, w.slot);
+      if (tracer) trace_event(tbi, kRoleEpilogue, kTraceItemEnd, w.tile, w.slot);
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
@@ -636,7 +647,8 @@ __global__ void __launch_bounds__(192, 1)
     __syncthreads();
   }
   // every role of the CTA (pair) is done: the end of the CTA's work
-  if (threadIdx.x == 0) trace_event(tb, 0, kTraceKernelEnd, -1, (int32_t)(clock64() & 0x7fffffff));
+  if (tb != nullptr && threadIdx.x == kStampThread)
+    trace_put(tb, stamp_slot + 1, globaltimer_ns(), 0, kTraceKernelEnd, -1, (int32_t)(clock64() & 0x7fffffff));
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc<CG>(tmem_base, S::TMEM_COLS);

@@ -481,7 +481,18 @@ __global__ void __launch_bounds__(192, 1)
   pdl_launch_dependents();
   pdl_wait_prior_grid();
   TraceBuf* const tb = args.trace;
-  if (threadIdx.x == 0) trace_event(tb, 0, kTraceKernelBegin, -1, (int32_t)(clock64() & 0x7fffffff));
+  TraceBuf* const tbi = args.trace_items ? tb : nullptr;  // work-item events (else only begin/end)
+  // This CTA's kernel begin and end records (with the SM cycle counter): both
+  // slots are reserved here by an epilogue thread, idle until the first
+  // accumulator is ready, so that neither the producer's first copy nor the
+  // CTA's exit waits for the trace's atomic.
+  unsigned long long stamp_slot = 0;
+  if (tb != nullptr && threadIdx.x == kStampThread) {
+    const uint64_t t = globaltimer_ns();
+    const int32_t clk = (int32_t)(clock64() & 0x7fffffff);
+    stamp_slot = trace_reserve(tb, 2ull);
+    trace_put(tb, stamp_slot, t, 0, kTraceKernelBegin, -1, clk);
+  }
 
   if (warp == 0) {
     // ---------------------------------------------------- TMA producer ----
@@ -496,7 +507,7 @@ __global__ void __launch_bounds__(192, 1)
         const int more = feed.next(sg, ctl);
         if (more < 0) ok = false;
         if (more <= 0) break;
-        trace_event(tb, kRoleProducer, kTraceItemBegin, sg.tile, sg.kb0);
+        trace_event(tbi, kRoleProducer, kTraceItemBegin, sg.tile, sg.kb0);
         if (args.checks && (sg.tile < 0 || sg.tile >= args.n_tiles || sg.kb0 < 0 || sg.kb0 >= sg.kb1 ||
                             sg.kb1 > args.k_blocks || sg.chunk < 0 || sg.chunk >= chunks.count())) {
           report_check(args.status, kCheckItem, abort_flag);
@@ -533,7 +544,7 @@ __global__ void __launch_bounds__(192, 1)
           }
         }
       }
-      trace_event(tb, kRoleProducer, kTraceItemEnd, -1, (int32_t)issued);
+      trace_event(tbi, kRoleProducer, kTraceItemEnd, -1, (int32_t)issued);
       if (!ok) sk_report(args.status, kRoleProducer, abort_flag);
       if (!feed.clc.drain(drain_ctl)) sk_report(args.status, kRoleTeardown, abort_flag);
       for (int s = 0; s < stages; ++s) {
@@ -564,7 +575,7 @@ __global__ void __launch_bounds__(192, 1)
           break;
         }
         tc_fence_after();
-        trace_event(tb, kRoleMma, kTraceItemBegin, sg.tile, sg.kb0);
+        trace_event(tbi, kRoleMma, kTraceItemBegin, sg.tile, sg.kb0);
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * mma_n);
         for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
           if (!mbar_wait(full_bar(stage), phase, ctl)) {
@@ -594,7 +605,7 @@ __global__ void __launch_bounds__(192, 1)
         }
         if (!ok) break;
         tc_commit(tfull_bar(acc));
-        trace_event(tb, kRoleMma, kTraceItemEnd, sg.tile, sg.kb1);
+        trace_event(tbi, kRoleMma, kTraceItemEnd, sg.tile, sg.kb1);
         if (++acc == nacc) {
           acc = 0;
           acc_phase ^= 1u;
@@ -682,7 +693,7 @@ __global__ void __launch_bounds__(192, 1)
         break;
       }
       tc_fence_after();
-      if (threadIdx.x == 64) trace_event(tb, kRoleEpilogue, kTraceItemBegin, sg.tile, sg.kb0);
+      if (threadIdx.x == 64) trace_event(tbi, kRoleEpilogue, kTraceItemBegin, sg.tile, sg.kb0);
       float v[kSplitKMaxM];
       const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * mma_n);
 #pragma unroll
@@ -732,7 +743,7 @@ __global__ void __launch_bounds__(192, 1)
           if (threadIdx.x == 64) *ticket_slot = atom_add_acq_rel_gpu(arrivals, 1);  // ... before the ticket
           named_bar_sync(1, 128);  // ... and the acquire orders the partial reads below
           const int32_t ticket = *ticket_slot;
-          if (threadIdx.x == 64) trace_event(tb, kRoleEpilogue, kTracePartialStored, sg.tile, ticket);
+          if (threadIdx.x == 64) trace_event(tbi, kRoleEpilogue, kTracePartialStored, sg.tile, ticket);
           if (args.checks && threadIdx.x == 64 && (ticket < 0 || ticket > others))
             report_check(args.status, kCheckTicket, abort_flag);
           last = (ticket == others);
@@ -750,12 +761,12 @@ __global__ void __launch_bounds__(192, 1)
           store_tile(cstage, s, row, args.M, args.N, sg.tile, args.C, out_bf16);
           if (threadIdx.x == 64) {
             *arrivals = 0;  // ready for the next launch
-            trace_event(tb, kRoleEpilogue, kTraceReduced, sg.tile, others + 1);
+            trace_event(tbi, kRoleEpilogue, kTraceReduced, sg.tile, others + 1);
           }
         }
         named_bar_sync(1, 128);  // ticket_slot and watch_slot are reused by the next segment
       }
-      if (threadIdx.x == 64) trace_event(tb, kRoleEpilogue, kTraceItemEnd, sg.tile, sg.kb1);
+      if (threadIdx.x == 64) trace_event(tbi, kRoleEpilogue, kTraceItemEnd, sg.tile, sg.kb1);
     }
     cp_async_wait_all();  // copies a segment that gave up had in flight
     if (!ok && lane == 0) sk_report(args.status, kRoleEpilogue, abort_flag);
@@ -763,7 +774,8 @@ __global__ void __launch_bounds__(192, 1)
 
   __syncthreads();
   // every role of the CTA is done: the end of the CTA's work
-  if (threadIdx.x == 0) trace_event(tb, 0, kTraceKernelEnd, -1, (int32_t)(clock64() & 0x7fffffff));
+  if (tb != nullptr && threadIdx.x == kStampThread)
+    trace_put(tb, stamp_slot + 1, globaltimer_ns(), 0, kTraceKernelEnd, -1, (int32_t)(clock64() & 0x7fffffff));
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc<1>(tmem_base, (uint32_t)tmem_cols);

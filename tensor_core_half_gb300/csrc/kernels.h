@@ -41,6 +41,11 @@ struct TraceBuf {
   TraceRecord rec[1];
 };
 
+// Thread that records each CTA's kernel begin/end trace events: lane 0 of the
+// first epilogue warp (both kernels run a producer warp, an MMA warp, then
+// the epilogue warps).
+constexpr int kStampThread = 64;
+
 // Default limit of every bounded device-side wait.
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 // Limit used when draining in-flight copies after another role gave up.
@@ -67,6 +72,7 @@ struct DenseArgs {
   uint64_t timeout_ns;
   int32_t* status;
   TraceBuf* trace;         // null unless tracing
+  int32_t trace_items;     // 1: trace every event kind; 0: only each CTA's kernel begin/end
 };
 
 enum DenseKind : int { kDense1Sm128 = 0, kDense1Sm256 = 1, kDense2Sm256 = 2, kDense2Sm192 = 3 };
@@ -111,6 +117,7 @@ struct SplitKArgs {
   int32_t ticket_stride;  // int32 words between counters: kSplitKTicketStride (one 128-byte line each), or 1
   void* C;           // [M][N] row-major
   TraceBuf* trace;   // null unless tracing
+  int32_t trace_items;  // 1: trace every event kind; 0: only each CTA's kernel begin/end
 };
 
 constexpr int kSplitKMaxM = 64;

@@ -214,5 +214,6 @@ extern "C" hgemm_status_t hgemm_run_splitk_noalloc(const void* A, const void* B,
   args.partials = reinterpret_cast<float*>(d->scratch + kPartialOffset);
   args.C = C;
   args.trace = nullptr;
+  args.trace_items = 0;
   return hg::splitk_launch(tmW, tmX, args, (int)grid, smem, s) == cudaSuccess ? HGEMM_OK : HGEMM_ERR_CUDA;
 }

@@ -470,20 +470,31 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 // ------------------------------------------------------------ tracing ----
-// Appends one event to a trace buffer (see kernels.h); no-op for a null buffer.
+// Reserves n consecutive records of a trace buffer (see kernels.h) and returns
+// the first index, which may lie past the capacity (those records are dropped).
 template <class Buf>
-__device__ __forceinline__ void trace_event(Buf* tb, uint16_t role, uint16_t kind, int32_t item, int32_t value) {
-  if (tb == nullptr) return;
-  const unsigned long long i = atomicAdd(&tb->count, 1ull);
+__device__ __forceinline__ unsigned long long trace_reserve(Buf* tb, unsigned long long n) {
+  return atomicAdd(&tb->count, n);
+}
+// Writes one event into reserved record i (plain stores: nothing waits for them).
+template <class Buf>
+__device__ __forceinline__ void trace_put(Buf* tb, unsigned long long i, uint64_t t_ns, uint16_t role, uint16_t kind,
+                                          int32_t item, int32_t value) {
   if (i < tb->capacity) {
     auto& r = tb->rec[i];
-    r.t_ns = globaltimer_ns();
+    r.t_ns = t_ns;
     r.cta = blockIdx.x;
     r.role = role;
     r.kind = kind;
     r.item = item;
     r.value = value;
   }
+}
+// Appends one event; no-op for a null buffer.
+template <class Buf>
+__device__ __forceinline__ void trace_event(Buf* tb, uint16_t role, uint16_t kind, int32_t item, int32_t value) {
+  if (tb == nullptr) return;
+  trace_put(tb, trace_reserve(tb, 1ull), globaltimer_ns(), role, kind, item, value);
 }
 
 }  // namespace hg

@@ -67,6 +67,7 @@ HGEMM_EPILOGUE_TMA_STORE = 0
 HGEMM_EPILOGUE_DIRECT = 1
 EPILOGUES = {"tma": HGEMM_EPILOGUE_TMA_STORE, "direct": HGEMM_EPILOGUE_DIRECT}
 HGEMM_OPT_CHECKS = 10
+HGEMM_OPT_TRACE_ITEMS = 11
 HGEMM_ERR_CHECK = 9
 HGEMM_CHECK_WORK_ID, HGEMM_CHECK_ITEM, HGEMM_CHECK_TICKET, HGEMM_CHECK_CONTRIBUTOR, HGEMM_CHECK_PARTIAL = 1, 2, 3, 4, 5
 

@@ -35,6 +35,30 @@ def spans(rows):
     return out
 
 
+def launch_clocks(rows):
+    """SM clock (MHz) of every CTA launch in the records: each CTA's kernel
+    begin and end records, paired in time order, carry the global timer (ns)
+    and the low 31 bits of the SM cycle counter, so cycles / ns over the
+    pair is the clock that CTA ran at.  Works for records of many launches
+    (HGEMM_OPT_TRACE_ITEMS = 0 keeps only these records)."""
+    by = collections.defaultdict(list)
+    for t, cta, role, kind, item, value in rows:
+        if role == 0 and kind in (1, 2):
+            by[cta].append((t, kind, value))
+    out = []
+    for ev in by.values():
+        ev.sort()
+        begin = None
+        for t, kind, value in ev:
+            if kind == 1:
+                begin = (t, value)
+            elif begin is not None:
+                if t > begin[0]:
+                    out.append(((value - begin[1]) % (1 << 31)) / (t - begin[0]) * 1e3)
+                begin = None
+    return out
+
+
 def summary(rows):
     """Kernel span, per-role busy time and the spread of CTA end times (ns)."""
     if not rows:

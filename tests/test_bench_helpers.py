@@ -144,3 +144,23 @@ def test_secondary_workloads_cover_the_targets():
     assert "square8192_bf16" in bench.SECONDARY and "skinny16x16384x8192_bf16" in bench.SECONDARY
     assert bench.workload_metric(workloads.WORKLOADS["skinny16x16384x8192_bf16"])[3] == "hbm"
     assert bench.workload_metric(workloads.WORKLOADS["square8192_bf16"])[3] == "tensor"
+
+
+def test_in_kernel_clocks_pair_each_ctas_begin_and_end():
+    """Two CTAs, three launches: each (begin, end) pair in time order gives
+    cycles / ns; the 31-bit cycle counter may wrap between the two."""
+    rows = []
+    t = 1_000_000
+    for launch in range(3):
+        for cta, mhz in ((0, 1800.0), (1, 2000.0)):
+            c0 = (2**31 - 50_000) if (launch == 1 and cta == 0) else 1_000 * (launch + 1)  # wraps in launch 1
+            dt = 80_000  # ns
+            rows.append((t, cta, 0, 1, -1, c0))
+            rows.append((t + dt, cta, 0, 2, -1, (c0 + int(mhz * dt / 1e3)) % 2**31))
+            rows.append((t + 10, cta, 3, 3, 5, 0))  # an item record is ignored
+        t += 100_000
+    rows.reverse()  # append order is not time order
+    c = bench.in_kernel_clocks(rows, len(rows), 12)
+    assert c["cta_launches"] == 6 and c["stamps"] == 18
+    assert c["sm_mhz_min"] == 1800.0 and c["sm_mhz_max"] == 2000.0
+    assert c["sm_mhz_median"] in (1800.0, 2000.0)

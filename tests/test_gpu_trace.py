@@ -188,3 +188,44 @@ def test_splitk_segments_in_plan_order(M, N, K):
             expect.append((tile, kb0))
             i += 1
         assert seen[c] == expect, c
+
+
+@pytest.mark.parametrize("variant,M,N,K,sk", [("2sm256", 4096, 2560, 4096, 3), ("1sm128", 1000, 3000, 2056, 2),
+                                              ("splitk", 16, 16384, 8192, 0)])
+def test_launch_stamps_only(variant, M, N, K, sk):
+    """HGEMM_OPT_TRACE_ITEMS = 0: every CTA of every launch records only its
+    kernel begin and end, whose cycle-counter and timer values give the SM
+    clock each CTA ran at; the launches compute the same bits as an untraced
+    one, which matches the oracle on sampled entries."""
+    launches = 3
+    a, b, ab, bb = parity.inputs(M, N, K, "TN", "bf16", ("normal", 1.0), 76)
+    A, B = a.cuda(), b.cuda()
+    C0 = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    Cs = [torch.empty_like(C0) for _ in range(launches)]
+    with hgemm.Handle() as h:
+        h.set_option(hgemm.HGEMM_OPT_FORCE_VARIANT, hgemm.VARIANTS[variant])
+        h.set_option(hgemm.HGEMM_OPT_STREAM_K, sk)
+        h.run(A, B, C0, layout="TN", acc="f32")
+        h.set_option(hgemm.HGEMM_OPT_TRACE, 1 << 16)
+        h.set_option(hgemm.HGEMM_OPT_TRACE_ITEMS, 0)
+        for C in Cs:
+            h.run(A, B, C, layout="TN", acc="f32")
+        st, detail = h.sync_status()
+        assert st == hgemm.HGEMM_OK, (st, hex(detail))
+        st, n, rows = hgemm.hgemm_trace_read(h.h, 1 << 16)
+        assert st == hgemm.HGEMM_OK and n == len(rows)
+        assert hgemm.hgemm_set_option(h.h, hgemm.HGEMM_OPT_TRACE_ITEMS, 2) == hgemm.HGEMM_ERR_INVALID_ARG
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    st, p = hgemm.hgemm_plan(M, N, K, 0, hgemm.HGEMM_BF16, hgemm.HGEMM_F32, hgemm.HGEMM_BF16, sms,
+                             hgemm.VARIANTS[variant], 0, sk)
+    assert n == 2 * p.grid * launches
+    assert all(r[2] == 0 and r[3] in (1, 2) for r in rows)
+    per_cta = collections.Counter((r[1], r[3]) for r in rows)
+    assert len(per_cta) == 2 * p.grid and set(per_cta.values()) == {launches}
+    mhz = trace.launch_clocks(rows)
+    assert len(mhz) == p.grid * launches
+    assert 200.0 < sorted(mhz)[len(mhz) // 2] < 4000.0
+    for C in Cs:
+        assert torch.equal(C.view(torch.int16), C0.view(torch.int16))
+    got = C0.view(torch.int16).cpu().numpy().view("uint16")
+    parity.check(got, ab, bb, M, N, K, "TN", "bf16", "f32", "bf16", sampled=True, n_random=4096, seed=3)

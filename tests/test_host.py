@@ -20,6 +20,20 @@ def test_library_exports_every_declared_symbol():
     assert not missing, missing
 
 
+def test_binding_constants_match_the_header():
+    """Every enumerator include/hgemm.h declares has a binding constant of the
+    same name and value (the binding restates them; a stale copy would pass
+    the wrong option or status to the library)."""
+    import pathlib
+    import re
+
+    text = (pathlib.Path(__file__).resolve().parents[1] / "include" / "hgemm.h").read_text()
+    declared = re.findall(r"(?m)^\s*(HGEMM_[A-Za-z0-9_]+)\s*=\s*(-?\d+)", text)
+    assert len(declared) >= 39 and any(n == "HGEMM_OPT_TRACE_ITEMS" for n, _ in declared)
+    wrong = [(n, v, getattr(H, n, None)) for n, v in declared if getattr(H, n, None) != int(v)]
+    assert not wrong, wrong
+
+
 def test_status_strings():
     for s in range(0, 10):
         assert H.hgemm_status_string(s).startswith("HGEMM_")
