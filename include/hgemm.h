@@ -97,10 +97,11 @@ typedef enum {
                                   slots in range) and report a violation as HGEMM_ERR_CHECK
                                   instead of trapping; 0 (default) = no checks              */
   HGEMM_OPT_TRACE_ITEMS = 11   /* value: 1 (default) = the trace (HGEMM_OPT_TRACE) records every
-                                  event kind; 0 = only each CTA's kernel begin and end records
-                                  (two per CTA per launch: the SM cycle counter against the
-                                  global timer, i.e. the SM clock during each launch, at the
-                                  cost of two appends per CTA)                               */
+                                  event kind; 0 = only each CTA's kernel begin and end records,
+                                  two per CTA per launch, whose SM cycle counter and global
+                                  timer give the SM clock of every launch (both records are
+                                  reserved by one atomic of a thread that is idle then, so no
+                                  role of the kernel waits on the trace)                     */
 } hgemm_option_t;
 
 /* Check numbers reported with HGEMM_ERR_CHECK (detail bits 8-15). */
