@@ -83,7 +83,8 @@ def load_peaks():
 
 def load_traffic(workload: str, variant: int, plan=None):
     """DRAM bytes per launch from a committed ncu summary, if it matches these
-    kernels and this launch plan (the stream-K split changes the traffic)."""
+    kernels and this launch plan (the stream-K split and the rasterisation
+    height change the traffic)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -96,7 +97,7 @@ def load_traffic(workload: str, variant: int, plan=None):
     want = e.get("plan")
     if plan is not None and want is not None:
         have = {"grid": plan.grid, "dp_tiles": plan.dp_tiles, "sk_units": plan.sk_units,
-                "sk_ranges": plan.sk_ranges}
+                "sk_ranges": plan.sk_ranges, "group_m": getattr(plan, "group_m", None)}
         if any(have[k] != v for k, v in want.items()):
             return None
     return e.get("dram_bytes_per_launch")

@@ -75,7 +75,9 @@ typedef enum {
                                   host fills the fix-up ticket counters with 0x01 bytes before
                                   a stream-K or split-K launch, which HGEMM_OPT_CHECKS must
                                   report (tests)                                              */
-  HGEMM_OPT_GROUP_M = 4,       /* value: rasterisation group height in tiles (default 8)      */
+  HGEMM_OPT_GROUP_M = 4,       /* value: rasterisation group height in tiles; 0 (default) =
+                                  automatic: every tile row when all of A fits in 32 MiB
+                                  (A then stays in L2), else 8                             */
   HGEMM_OPT_MAX_CTAS = 5,      /* value: cap on persistent CTAs (0 = one per SM)              */
   HGEMM_OPT_STREAM_K = 6,      /* value: 1 (default) lets the planner split the last wave of
                                   dense tiles along K (stream-K) when its estimate favours it;
@@ -303,7 +305,7 @@ typedef struct {
  * hgemm_plan -- the launch plan hgemm_run would use for these arguments on a
  * GPU with `num_sms` SMs (cluster capacity assumed num_sms / 2 pairs).
  * `variant` = HGEMM_VARIANT_AUTO or a forced variant; group_m = 0 for the
- * default; stream_k = 1 to allow stream-K, 0 to forbid it, 2 to force equal
+ * automatic height (as HGEMM_OPT_GROUP_M); stream_k = 1 to allow stream-K, 0 to forbid it, 2 to force equal
  * ranges, 3 to force equal K pieces (as HGEMM_OPT_STREAM_K).  Validates the
  * sizes, dtypes and layout like hgemm_run (pointers are not involved).
  */

@@ -29,6 +29,7 @@ namespace {
 
 constexpr int32_t kVersion = 100;
 constexpr int kDefaultGroupM = 8;
+constexpr int64_t kWholeABytes = 32ll << 20;  // A up to this size is read from HBM once (one group)
 constexpr int kDefaultSmemOptin = 232448;  // 227 KiB, sm_100-class parts
 constexpr int64_t kMaxDim = 2147483647;
 
@@ -45,7 +46,7 @@ struct Ctx {
   int force_variant = HGEMM_VARIANT_AUTO;
   uint64_t timeout_ns = kDefaultTimeoutNs;
   int inject = 0;
-  int group_m = kDefaultGroupM;
+  int group_m = 0;  // 0: auto_group_m
   int max_ctas = 0;
   int stream_k = 1;  // 0 never, 1 when the estimate says so, 2 whenever the tile count leaves a partial wave
   int schedule = HGEMM_SCHEDULE_STATIC;
@@ -216,6 +217,22 @@ DenseChoice dense_choice(DenseKind kind, int64_t M, int64_t N, int64_t K, int ca
   return best;
 }
 
+// Rasterisation group height when the caller sets none.  Tiles are visited
+// in groups of group_m tile rows, down the rows of a group column by column,
+// so a wave of clusters reads the A rows of one group and a few tile columns
+// of B.  When all of A fits in 32 MiB, one group spans every tile row: A then
+// stays in L2 and is read from HBM once, and the waves stream B once (4096^3
+// bf16 on GB300: 96 MB of DRAM traffic per launch instead of 131 MB, and 0.6-
+// 1.4 % faster, the lower DRAM power leaving the SMs a higher clock).  Larger
+// A keeps 8 tile rows: from K = 8192 to 16384 (8192^3, 12288^3, 16384^3,
+// 8192 x 8192 x 16384) heights of 4-5 measured 1-2 % slower and 16-32 up to
+// 10 % slower, their extra DRAM traffic lowering the clock under the power
+// limit.
+int auto_group_m(int64_t M, int64_t K, int32_t tiles_m) {
+  if (M * K * 2 <= kWholeABytes && tiles_m > kDefaultGroupM) return tiles_m;
+  return kDefaultGroupM;
+}
+
 void fill_dense_plan(DenseKind kind, const DenseChoice& ch, int64_t M, int64_t N, int64_t K, int group_m,
                      hgemm_plan_t* p) {
   const DenseKindInfo info = dense_kind_info(kind);
@@ -230,7 +247,7 @@ void fill_dense_plan(DenseKind kind, const DenseChoice& ch, int64_t M, int64_t N
   p->num_tiles = p->tiles_m * p->tiles_n;
   p->k_blocks = (int32_t)cdiv(K, 64);
   p->grid = ch.clusters * info.cta_group;
-  p->group_m = group_m > 0 ? group_m : kDefaultGroupM;
+  p->group_m = group_m > 0 ? group_m : auto_group_m(M, K, p->tiles_m);
   p->smem_bytes = info.smem_bytes;
   p->tmem_cols = info.tmem_cols;
   p->dp_tiles = ch.dp_tiles;
@@ -608,7 +625,7 @@ hgemm_status_t hgemm_set_option(hgemm_handle_t h, int32_t option, int64_t value)
       h->inject = (int)value;
       return HGEMM_OK;
     case HGEMM_OPT_GROUP_M:
-      if (value < 1 || value > 65536) return HGEMM_ERR_INVALID_ARG;
+      if (value < 0 || value > 65536) return HGEMM_ERR_INVALID_ARG;
       h->group_m = (int)value;
       return HGEMM_OK;
     case HGEMM_OPT_MAX_CTAS:

@@ -118,6 +118,20 @@ def test_plan_variant_choice():
     assert (p.tiles_m, p.tiles_n, p.k_blocks) == (8, 24, 65)
 
 
+def test_automatic_group_height():
+    # All of A within 32 MiB: one group spans every tile row (A read from HBM once).
+    assert plan(4096, 4096, 4096)[1].group_m == 16
+    assert plan(6144, 4096, 2048)[1].group_m == 24
+    assert plan(4096, 4096, 4096, fin=0, acc=0, out=0)[1].group_m == 16
+    # Larger A, or no more than 8 tile rows: 8.
+    assert plan(8192, 8192, 8192)[1].group_m == 8
+    assert plan(4096, 4096, 4104)[1].group_m == 8  # A just over 32 MiB
+    assert plan(2048, 2048, 2048)[1].group_m == 8
+    assert plan(1000, 3000, 4104)[1].group_m == 8
+    # An explicit height is kept.
+    assert plan(4096, 4096, 4096, group_m=4)[1].group_m == 4
+
+
 @pytest.mark.parametrize("M,N,K,variant", [(4096, 4096, 4096, 3), (1000, 3000, 4104, 1), (1000, 3000, 4104, 2),
                                            (8192, 8192, 64, 3), (129, 8, 8, 3), (5000, 136, 64, 1)])
 @pytest.mark.parametrize("group_m", [1, 3, 8, 100])
