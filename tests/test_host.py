@@ -150,15 +150,21 @@ def test_tile_map_is_a_bijection(M, N, K, variant, group_m):
 
 def test_tile_map_groups_rows():
     # Within a full group, consecutive tiles walk down group_m tile rows before
-    # moving one tile column right ("block swizzle" band order).
+    # moving one tile column on ("block swizzle" band order).
     st, p = plan(4096, 4096, 4096, variant=3, group_m=4)
     coords = [H.hgemm_plan_tile(p, t)[1:] for t in range(12)]
     assert coords[:5] == [(0, 0), (1, 0), (2, 0), (3, 0), (0, 1)]
     assert coords[8] == (0, 2)
+    # odd groups walk the tile columns right to left (serpentine), so a group
+    # starts on the columns its predecessor read last
+    second = [H.hgemm_plan_tile(p, t)[1:] for t in range(4 * 16, 4 * 16 + 6)]
+    assert second == [(4, 15), (5, 15), (6, 15), (7, 15), (4, 14), (5, 14)]
+    third = H.hgemm_plan_tile(p, 8 * 16)[1:]
+    assert third == (8, 0)
     # the last group is shorter when tiles_m is not a multiple of group_m
     st, p = plan(5 * 256, 512, 64, variant=3, group_m=4)
     tail = [H.hgemm_plan_tile(p, t)[1:] for t in range(8, 10)]
-    assert tail == [(4, 0), (4, 1)]
+    assert tail == [(4, 1), (4, 0)]
 
 
 @pytest.mark.parametrize("M,N,K,sms", [(16, 16384, 8192, 152), (1, 8, 64, 152), (64, 1000, 72, 152),
