@@ -842,6 +842,7 @@ def sweep(args):
                                         "peak_source": "%s%s" % (peak_src, " burst" if bound == "tensor" else "")},
                            "plan": {"variant": list(hgemm.VARIANTS)[plan.variant], "grid": plan.grid,
                                     "tile": [plan.tile_m, plan.tile_n], "stages": plan.stages,
+                                    "group_m": plan.group_m,
                                     "stream_k": bool(plan.stream_k), "sk_pieces": plan.sk_pieces,
                                     "sk_ranges": plan.sk_ranges, "work_ids": plan.work_ids,
                                     "splitk_chunks": plan.splitk_chunks,
