@@ -340,7 +340,8 @@ hgemm_status_t hgemm_plan_id_item(const hgemm_plan_t* plan, int32_t id, int32_t 
 /*
  * hgemm_plan_tile -- the persistent scheduler's map from a linear tile index
  * (0 <= t < plan->num_tiles) to tile coordinates: grouped rasterisation,
- * group_m tile rows swept together along N.  The same function runs on the
+ * group_m tile rows swept together along N, even groups left to right and
+ * odd groups right to left (serpentine).  The same function runs on the
  * device.  For split-K plans, tile t is the t-th block of 128 rows of N.
  */
 hgemm_status_t hgemm_plan_tile(const hgemm_plan_t* plan, int32_t t, int32_t* tile_m_idx, int32_t* tile_n_idx);
