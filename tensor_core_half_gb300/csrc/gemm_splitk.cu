@@ -101,18 +101,20 @@ namespace {
 // GB300 streaming rates behind the layout choice (a CTA streaming B tiles
 // along K through an 11-stage ring, measured with 32-152 CTAs): one CTA
 // reaches 62-68 GB/s, and the GPU as a whole about 6250 GB/s, which about 100
-// CTAs already reach.  Whole tiles keep ~94 % of that in the kernel (one
-// tile per CTA, so the slowest SM ends the launch: 128 CTAs measured 5.75
-// TB/s where the balanced split streams 6.2).  A split of some tile's K
-// range between CTAs costs the fix-up at the end of the kernel: ~4 us at
-// M <= 16 (16 x 16384 x 8192, the same launches with the fix-ups left out),
-// growing with the fp32 partials, ~1.5 us per further 16 columns of M.
-// Measured choices this reproduces: whole tiles at 16 x 16384 x 8192,
-// 16 x 12288 x 8192, 32 x 14336 x 4096 and 64 x 16384 x 8192; the split at
-// 16 x 20480 x 8192, 16 x 8192 x 8192 and 1 x 16384 x 16384.
+// CTAs already reach.  Whole tiles, their K walks started at eight offsets
+// (SegmentOrder), keep all of that in the kernel (128 CTAs: 6.3-6.5 TB/s of
+// streaming; 0.94 of it while every tile walked K from its start).  A split
+// of some tile's K range between CTAs costs the fix-up at the end of the
+// kernel: ~4 us at M <= 16 (16 x 16384 x 8192, the same launches with the
+// fix-ups left out), growing with the fp32 partials, ~1.5 us per further 16
+// columns of M.  Measured choices this reproduces (the faster layout, timed
+// both ways on one box): whole tiles at 16 x 16384 x 8192, 16 x 12288 x 8192,
+// 32 x 14336 x 4096, 64 x 16384 x 8192, 16 x 32768 x 4096, 4 x 32768 x 8192
+// and {1, 8, 16} x 16384 x 16384; the split at 16 x 20480 x 8192,
+// 16 x 8192 x 8192 and 1 x 8192 x 16384.
 constexpr double kSplitKCtaGBs = 62.0;
 constexpr double kSplitKGpuGBs = 6250.0;
-constexpr double kSplitKWholeEff = 0.94;
+constexpr double kSplitKWholeEff = 1.0;
 constexpr double kSplitKFixupNs = 4000.0;
 constexpr double kSplitKFixupPer16Ns = 1500.0;
 constexpr int kSplitKSplitStages = 5;  // 180 KB in flight at M <= 16

@@ -196,7 +196,9 @@ def test_splitk_partition(M, N, K, sms):
     (16, 16384, 8192, 148, True, 128),
     (64, 16384, 8192, 152, True, 128),    # the split's fix-up grows with M
     (32, 14336, 4096, 152, True, 112),
-    (1, 16384, 16384, 152, False, 152)])  # long K: the slowest SM's share of a whole tile outweighs the fix-up
+    (1, 16384, 16384, 152, True, 128),    # long K: whole tiles stream as fast as all SMs, with no fix-up
+    (4, 32768, 8192, 152, True, 128),     # 256 tiles: two per CTA
+    (1, 8192, 16384, 152, False, 152)])   # 64 tiles: 64 CTAs would stream at ~4 TB/s
 def test_splitk_whole_tile_choice(M, N, K, sms, whole, grid):
     """The planner's layout for skinny products: whole tiles per CTA (no
     tile's K range split, no fix-up) when 128-row tiles at the CTA count that
