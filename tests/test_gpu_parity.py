@@ -244,6 +244,23 @@ def test_splitk_dynamic_small_integers_bit_exact(h):
     assert np.array_equal(got, ref)
 
 
+@pytest.mark.parametrize("M,K", [(16, 1032), (33, 4104), (5, 520)])
+def test_splitk_whole_tiles_ragged_k_from_every_offset(h, M, K):
+    # Whole tiles walk K from (tile mod 8)/8 of their k-blocks and wrap, so with
+    # a ragged K the short last k-block (zero-filled past K) falls in the middle
+    # of most tiles' walks; 128 tiles cover all eight offsets.
+    N = 16384
+    st, p = hgemm.hgemm_plan(M, N, K, num_sms=torch.cuda.get_device_properties(0).multi_processor_count, stream_k=0)
+    assert p.variant == hgemm.HGEMM_VARIANT_SPLITK and p.splitk_align == p.k_blocks and K % 128 != 0
+    a, b, ab, bb = parity.inputs(M, N, K, "TN", "bf16", ("normal", 1.0), 94)
+    got = run(h, a, b, M, N, K, "TN", "f32", "bf16", "splitk", stream_k=0)
+    parity.check(got, ab, bb, M, N, K, "TN", "bf16", "f32", "bf16")
+    a, b, ab, bb = parity.inputs(M, N, K, "TN", "bf16", ("int", -4, 4), 95)
+    got = run(h, a, b, M, N, K, "TN", "f32", "bf16", "splitk", stream_k=0)
+    ref, _, _ = oracle.gemm(ab, bb, M, N, K, "TN", "bf16", "bf16")
+    assert np.array_equal(got, ref)
+
+
 def test_splitk_small_integers_bit_exact(h):
     M, N, K = 16, 2048, 4096
     a, b, ab, bb = parity.inputs(M, N, K, "TN", "f16", ("int", -4, 4), 23)
